@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the Skip-Softmax (BLASST) attention forward on GB300.
+
+One step = one call of ``blasst_attn_fwd`` (the whole hot path: Q K^T for every
+tile pair, the per-tile skip test, softmax and P V for kept tiles, epilogue) on
+the Wan-shaped self-attention workload: B=1, H=40, Sq=Sk=32760 (a 21 x 30 x 52
+latent grid, cells 3 x 6 x 6), d=128, bf16, seeded synthetic clustered inputs.
+
+The JSON line reports dense-equivalent TFLOPS (4 B H Sq Sk d / time) at the
+headline factor, with ms/call, the skip fraction and executed TFLOPS for every
+factor of the workload's sweep, the tensor-core roofline of the kernel, the
+end-to-end number through the C ABI with host buffers, and the CPU oracle's
+throughput on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--factor F]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "ms/call and dense-equiv TFLOPS vs skip fraction, bf16 d=128, S=32760, 1×GB300"
+UNIT = "TFLOPS (dense-equivalent)"
+TILE = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="wan_32760", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--factor", type=float, default=None, help="headline factor (default: largest of the sweep)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-units", type=int, default=16, help="query tiles in the CPU oracle sample")
+    return ap.parse_args()
+
+
+def workload_factors(w):
+    if w.curve is not None:
+        a, b, ts = w.curve
+        return [0.0] + [a * math.exp(b * t) for t in ts]
+    return list(w.factors)
+
+
+def dense_flops(w):
+    return 4.0 * w.B * w.H * w.S * w.S * w.d
+
+
+def executed_flops(w, mask):
+    """2 r c d per QK^T tile pair, plus the same for P V on kept pairs (r, c = valid rows / keys)."""
+    nQ, nK = mask.shape[-2], mask.shape[-1]
+    r = np.minimum(TILE, w.S - TILE * np.arange(nQ)).astype(np.float64)
+    c = np.minimum(TILE, w.S - TILE * np.arange(nK)).astype(np.float64)
+    rc = np.outer(r, c)
+    kept = 1.0 - mask.reshape(-1, nQ, nK).astype(np.float64)
+    return float((2.0 * w.d * rc[None] * (1.0 + kept)).sum())
+
+
+def sample_units(w, n):
+    """The first query tiles of the first and last head (batch 0): a bounded CPU sample."""
+    per_head = max(1, n // 2)
+    heads = (0, w.H - 1) if w.H > 1 else (0,)
+    nQ = -(-w.S // TILE)
+    return np.array([(0, h, t) for h in heads for t in range(min(per_head, nQ))], dtype=np.int32)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "of measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_rate(w, q, k, v, factor, n_units, threads):
+    """Dense-equivalent TFLOPS of the CPU oracle on a bounded sample of query tiles."""
+    import oracle
+    units = sample_units(w, n_units)
+    scale = 1.0 / math.sqrt(w.d)
+    t0 = time.perf_counter()
+    oracle.skip_softmax_attn(q, k, v, scale, factor, units=units, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = sum(4.0 * min(TILE, w.S - TILE * int(t)) * w.S * w.d for _, _, t in units)
+    return flops / dt / 1e12, dt, units
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle, as it stands, timed on the host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    q, k, v = synth.make_qkv(w)
+    factor = args.factor if args.factor is not None else max(workload_factors(w))
+    threads = os.cpu_count() or 1
+    n_units = max(1, min(threads, 8))
+    units = sample_units(w, n_units)
+    scale = 1.0 / math.sqrt(w.d)
+    for _ in range(args.warmup):
+        oracle.skip_softmax_attn(q, k, v, scale, factor, units=units[:1], threads=1)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.skip_softmax_attn(q, k, v, scale, factor, units=units, threads=threads)
+        times.append(time.perf_counter() - t0)
+    flops = sum(4.0 * min(TILE, w.S - TILE * int(t)) * w.S * w.d for _, _, t in units)
+    value = flops * args.steps / sum(times) / 1e12
+    sample = (f"{len(units)} query tiles of {w.name} (batch 0, heads 0 and {w.H - 1}, first tiles) "
+              f"per step at factor {factor:g}, fp64 scalar C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded clustered video-DiT token grid)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "d": w.d, "factor": factor,
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_calls(blasst, stream, args_fn, n):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n):
+            args_fn()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / n  # ms per call
+
+
+def run_ours(args, w):
+    import torch
+
+    import softmax_threshold_tile_gb300 as blasst
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    blasst.build_library()
+    blasst.load_library()
+    factors = workload_factors(w)
+    head_factor = args.factor if args.factor is not None else max(factors)
+
+    q, k, v = synth.make_qkv(w)
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in (q, k, v))
+    B, S, H, d = w.B, w.S, w.H, w.d
+    nQ = -(-S // TILE)
+    od = torch.empty_like(qd)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    counts = torch.empty((B * H,), dtype=torch.int32, device="cuda")
+    mask = torch.empty((B, H, nQ, nQ), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    scale = 1.0 / math.sqrt(d)
+
+    def call(f, with_mask=False):
+        st = blasst.blasst_attn_fwd(qd, kd, vd, od, lse, B, H, S, S, d, scale, f, stream.cuda_stream,
+                                    counts, mask if with_mask else None)
+        if st != blasst.BLASST_OK:
+            raise blasst.BlasstError(st, "blasst_attn_fwd")
+
+    def mask_of(f):
+        with torch.cuda.stream(stream):
+            call(f, True)
+        stream.synchronize()
+        return mask.cpu().numpy()
+
+    peak_burst, _, peak_src = measured_peaks()
+    dense = dense_flops(w)
+
+    # ---- factor sweep (ms/call and TFLOPS vs skip fraction); not the contract's timed region
+    sweep = []
+    if not args.no_sweep:
+        n_sweep = max(3, args.steps // 2)
+        for f in factors:
+            m = mask_of(f)
+            for _ in range(args.warmup):
+                call(f)
+            ms = time_calls(blasst, stream, lambda: call(f), n_sweep)
+            skip = float(m.mean())
+            ex = executed_flops(w, m)
+            sweep.append({"factor": f, "lambda": f / S, "skip_fraction": skip, "ms": ms,
+                          "exec_tflops": ex / ms / 1e9, "dense_equiv_tflops": dense / ms / 1e9,
+                          "tensor_frac": ex / ms / 1e9 / peak_burst})
+        base = next((s["ms"] for s in sweep if s["factor"] == 0.0), None)
+        for s in sweep:
+            s["speedup_vs_dense"] = base / s["ms"] if base else None
+            s["bound"] = 1.0 / (1.0 - s["skip_fraction"] / 2.0)
+
+    # ---- the timed region: K calls at the headline factor
+    m = mask_of(head_factor)
+    skip = float(m.mean())
+    ex = executed_flops(w, m)
+    for _ in range(args.warmup):
+        call(head_factor)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            call(head_factor)
+        end.record(stream)
+        end.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    value = world * dense / (ms * 1e-3) / 1e12
+    achieved = ex / (ms_local * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q, k, v))
+        oh = torch.empty(od.shape, dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        ch = torch.empty(counts.shape, dtype=torch.int32).pin_memory()
+        n_e2e = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                qd.copy_(qh, non_blocking=True)
+                kd.copy_(kh, non_blocking=True)
+                vd.copy_(vh, non_blocking=True)
+                call(head_factor)
+                oh.copy_(od, non_blocking=True)
+                lh.copy_(lse, non_blocking=True)
+                ch.copy_(counts, non_blocking=True)
+
+        e2e_step()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        stream.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e = {"value": world * dense / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+               "steps": n_e2e,
+               "h2d_bytes_per_step": int(3 * q.nbytes),
+               "d2h_bytes_per_step": int(oh.numel() * 2 + lh.numel() * 4 + ch.numel() * 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = min(os.cpu_count() or 1, args.cpu_units)
+        rate, dt, units = cpu_oracle_rate(w, q, k, v, head_factor, args.cpu_units, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(units)} query tiles (batch 0, heads 0 and {w.H - 1}, first tiles) of "
+                         f"{w.name} at factor {head_factor:g}; {dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded clustered video-DiT token grid; replicas per GPU)",
+            "config": {"workload": w.name, "B": B, "H": H, "S": S, "d": d, "factor": head_factor,
+                       "lambda": head_factor / S, "skip_fraction": skip,
+                       "exec_tflops": achieved,
+                       "l2": f"inputs {3 * q.nbytes / 1e9:.2f} GB > 129 MB L2; no flush"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                         "frac": achieved / peak_burst, "traffic": None,
+                         "kernel": "blasst_fwd_sm103a", "peak_source": f"bf16 burst {peak_src}"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

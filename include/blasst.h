@@ -1,0 +1,100 @@
+/*
+ * blasst.h - C ABI of the GB300 (sm_103a) Skip-Softmax (BLASST) attention forward.
+ *
+ * The operation ("Skip-Softmax" design doc, vLLM-Omni, section "Algorithm";
+ * "Skip-Softmax" on docs.vllm.ai, sections "The online-softmax pass" and
+ * "The skip test"):
+ *
+ *   FlashAttention's single streaming pass over key tiles of 128. Per query row
+ *   it keeps m (largest score so far), l = sum exp(s - m) and O = sum exp(s - m) v
+ *   and returns O / l. For key tile j the scores S_j = Q . K_j^T . scale are
+ *   always computed. If, for EVERY query row i of the 128-row query tile,
+ *       tile_max[i] - running_max[i] < ln(lambda),
+ *   the tile's exponentials, its l / O update and its P . V product are dropped.
+ *   lambda = factor / Sk ("From configuration to the kernel threshold": the
+ *   kernel takes threshold_scale_factor and divides it by the KV length).
+ *   factor = 0 skips nothing and gives dense attention.
+ *
+ * Conventions for every entry point below:
+ *   - Tensors are contiguous, row-major, [B, S, H, d] for q / k / v / o (token
+ *     major, then head, then the d features), in bf16. lse is [B, H, Sq] fp32.
+ *   - d must be 128.
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device, owned
+ *     by the caller; the library keeps no reference after the call returns.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *     return once the work is enqueued. No call allocates device memory.
+ *   - Errors are reported by the return code only; nothing is enqueued when an
+ *     argument is rejected. No C++ exception crosses this interface.
+ */
+#ifndef BLASST_H_
+#define BLASST_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* a cudaStream_t is a `struct CUstream_st *` */
+
+typedef enum blasst_status {
+  BLASST_OK = 0,
+  BLASST_ERR_INVALID_ARG = 1,        /* an argument is outside the documented domain */
+  BLASST_ERR_UNSUPPORTED_DEVICE = 2, /* the current device is not compute capability 10.3 */
+  BLASST_ERR_LAUNCH = 3,             /* the CUDA runtime refused a launch, copy or set-up step */
+  BLASST_ERR_TIMEOUT = 4             /* a device-side wait gave up (see blasst_device_error) */
+} blasst_status;
+
+/*
+ * Skip-Softmax attention forward.
+ *
+ *   q            [B, Sq, H, 128] bf16, 16-byte aligned.
+ *   k, v         [B, Sk, H, 128] bf16, 16-byte aligned.
+ *   o            [B, Sq, H, 128] bf16 output, 16-byte aligned: O / l over the kept tiles.
+ *   lse          [B, H, Sq] fp32 output or NULL: m + ln(l) (natural log, scaled scores,
+ *                kept tiles only).
+ *   B, H         1 .. 65535.   Sq, Sk >= 1.   d == 128.
+ *   scale        score scale, finite and > 0 (typically 1/sqrt(128)).
+ *   factor       threshold_scale_factor, finite and >= 0; lambda = factor / Sk.
+ *   stream       CUDA stream the work is enqueued on.
+ *   skip_counts  [B * H] uint32 output or NULL: per (b, h), the number of
+ *                (query tile, key tile) pairs that were skipped. Overwritten
+ *                (zeroed on `stream`, then counted), never accumulated across calls.
+ *   skip_mask_dbg [B, H, ceil(Sq/128), ceil(Sk/128)] uint8 output or NULL: 1 where the
+ *                pair was skipped, 0 where it was computed. Every entry is written.
+ *
+ * Tiles are 128 query rows by 128 keys; key tiles are visited in ascending
+ * order; query rows past Sq do not vote and are not stored; keys past Sk are
+ * excluded from tile_max and from the softmax. The first key tile of every
+ * query tile is always computed.
+ *
+ * Returns BLASST_OK once enqueued, BLASST_ERR_INVALID_ARG (nothing enqueued),
+ * BLASST_ERR_UNSUPPORTED_DEVICE or BLASST_ERR_LAUNCH.
+ */
+blasst_status blasst_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int Sq, int Sk, int d, float scale, float factor,
+                              struct CUstream_st *stream, uint32_t *skip_counts,
+                              uint8_t *skip_mask_dbg);
+
+/* A static, human-readable name for a status code. */
+const char *blasst_status_string(blasst_status s);
+
+/*
+ * Reads the device-side error word of the current device, which a kernel sets
+ * when one of its bounded waits gives up (every wait in the kernel is limited
+ * in time; a kernel that gives up writes no further output and returns).
+ * Synchronizes the device. *word receives 0 when no wait gave up since the
+ * last clear; `clear` != 0 resets the word afterwards.
+ * Returns BLASST_OK, BLASST_ERR_TIMEOUT (word != 0), BLASST_ERR_INVALID_ARG
+ * (word == NULL) or BLASST_ERR_LAUNCH.
+ */
+blasst_status blasst_device_error(uint32_t *word, int clear);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int blasst_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLASST_H_ */

@@ -1,0 +1,112 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every workload of the benchmark table runs at its full size in the same launch
+configuration the benchmark times; the oracle checks sampled (b, h, query tile)
+units one by one, and properties that hold at any size are checked everywhere:
+skip counts equal the mask popcount, factor 0 skips nothing, the first key tile
+is never skipped, and skip sets grow with lambda (lambda <= 1).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import softmax_threshold_tile_gb300 as blasst
+    blasst.build_library()
+    blasst.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def _run_workload_sweep(w, factors, units, full_units=None):
+    q, k, v = synth.make_qkv(w)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    prev_mask = None
+    stats = []
+    for f in sorted(factors):
+        o, lse, counts, mask = parity.run_gpu(qd, kd, vd, f)
+        parity.check_counts(counts, mask, f)
+        if prev_mask is not None and f / w.S <= 1.0:
+            assert not np.any(prev_mask.astype(bool) & ~mask.astype(bool)), "skip set shrank as lambda grew"
+        prev_mask = mask
+        u = units if full_units is None or f not in full_units else full_units[f]
+        st = parity.compare_units(q, k, v, o, lse, mask, f, u)
+        st["factor"] = f
+        st["skip_fraction"] = float(mask.mean())
+        stats.append(st)
+    print(w.name, stats)
+    return stats
+
+
+def test_tiny_1024_every_unit():
+    w = synth.WORKLOADS["tiny_1024"]
+    units = parity.sample_units(w.B, w.H, w.S, heads=range(w.H), qtiles=range(w.S // 128))
+    stats = _run_workload_sweep(w, w.factors, units)
+    assert stats[0]["skipped"] == 0
+    assert stats[-1]["skipped"] > 0
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 1), (127, 127), (129, 129), (255, 255), (1000, 1000),
+                                   (300, 1000), (1000, 129), (128, 8), (8, 1000)])
+@pytest.mark.parametrize("factor", [0.0, 0.5, 4.0])
+def test_odd_shapes(Sq, Sk, factor):
+    q, k, v = parity.clustered_inputs(2, 3, Sq, Sk, seed=Sq * 7 + Sk)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    o, lse, counts, mask = parity.run_gpu(qd, kd, vd, factor)
+    parity.check_counts(counts, mask, factor)
+    units = parity.sample_units(2, 3, Sq, heads=range(3), qtiles=range(-(-Sq // 128)))
+    parity.compare_units(q, k, v, o, lse, mask, factor, units)
+
+
+def test_large_factor_lambda_above_one():
+    """lambda > 1 is allowed and computed literally (the decision is still the pages' test)."""
+    q, k, v = parity.clustered_inputs(1, 2, 512, 512, seed=11)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    f = 2048.0  # lambda = 4
+    o, lse, counts, mask = parity.run_gpu(qd, kd, vd, f)
+    parity.check_counts(counts, mask, f)
+    units = parity.sample_units(1, 2, 512, heads=range(2), qtiles=range(4))
+    parity.compare_units(q, k, v, o, lse, mask, f, units)
+
+
+@pytest.mark.parametrize("name", ["dit_8192_g1", "dit_8192_g2", "dit_8192_g3"])
+def test_dit_8192(name):
+    w = synth.WORKLOADS[name]
+    units = parity.sample_units(w.B, w.H, w.S, heads=(0, 11, 23), qtiles=(0, 1, 31, 63))
+    stats = _run_workload_sweep(w, w.factors, units)
+    assert stats[0]["skipped"] == 0
+
+
+def test_wan_32760():
+    w = synth.WORKLOADS["wan_32760"]
+    units = parity.sample_units(w.B, w.H, w.S, heads=(0, 20, 39), qtiles=(0, 1, 128, 255))
+    stats = _run_workload_sweep(w, w.factors, units)
+    assert stats[-1]["skip_fraction"] > 0
+
+
+def test_long_65536():
+    w = synth.WORKLOADS["long_65536"]
+    g = w.gammas()
+    heads = (0, 12, 23, int(np.argmin(g)), int(np.argmax(g)))
+    units = parity.sample_units(w.B, w.H, w.S, heads=heads, qtiles=(0, 255, 511))
+    _run_workload_sweep(w, w.factors, units)
+
+
+def test_ragged_37000():
+    w = synth.WORKLOADS["ragged_37000"]
+    a, b, ts = w.curve
+    factors = [0.0] + [a * math.exp(b * t) for t in ts]
+    units = parity.sample_units(w.B, w.H, w.S, heads=(0, 16, 31), qtiles=(0, 144, 289))
+    stats = _run_workload_sweep(w, factors, units)
+    assert stats[-1]["skip_fraction"] > 0
