@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-units", type=int, default=16, help="query tiles in the CPU oracle sample")
+    ap.add_argument("--cpu-units", type=int, default=48, help="query tiles in the CPU oracle sample")
     return ap.parse_args()
 
 
