@@ -8,19 +8,22 @@
 // tile's exponentials, its l / O update and its P V product are skipped.
 // lambda = factor / Sk ("From configuration to the kernel threshold").
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams all key
-// tiles through a warp-specialised pipeline:
-//   warps 0-3  softmax: one query row per thread (= TMEM lane). tcgen05.ld of
-//              S_j, row max, CTA-subset AND-vote on the skip test, exp2 of the
-//              kept tile written back into TMEM as bf16 P (aliasing S_j),
-//              conditional O rescale, epilogue (O / l -> bf16, lse).
-//   warp 4     MMA: one thread issues tcgen05.mma. S_{j+1} = Q K_{j+1}^T is
-//              issued before waiting for tile j's decision, so the tensor pipe
-//              computes the next scores while the softmax warps vote; then
-//              O += P_j V_j (A operand from TMEM) only for kept tiles.
-//   warp 5     TMA producer: Q once, K/V tiles through a 2-stage ring.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384).
-// Shared memory: Q 32 KiB, K 2 x 32 KiB, V 2 x 32 KiB, all 128-byte swizzled.
+// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and streams
+// every key tile once for both through a warp-specialised pipeline:
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one query row per
+//              thread (= TMEM lane). tcgen05.ld of S_j, row max, an AND-vote of
+//              the skip test over the tile's 128 rows (named barrier), exp2 of a
+//              kept tile written back into TMEM as bf16 P (over S_j), conditional
+//              O rescale, epilogue (O / l -> bf16, lse).
+//   warp 8     MMA: one thread issues tcgen05.mma, alternating the two tiles so
+//              that one tile's softmax overlaps the other tile's matrix work:
+//                O_A += P_A(j) V_j ; S_A = Q_A K_{j+1}^T ; O_B += P_B(j) V_j ; S_B = Q_B K_{j+1}^T
+//              P V is issued only for a tile that kept key tile j.
+//   warp 9     TMA producer: both Q tiles once, K tiles one ahead through a 2-stage ring,
+//              and V_j only once a tile has kept key tile j (as soon as tile A keeps it,
+//              otherwise after tile B's decision): a key tile both tiles skip is never loaded.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Shared memory: Q_A, Q_B, 2 x K, 2 x V tiles of 32 KiB, all 128-byte swizzled.
 //
 // Numerics: scores are fp32 from bf16 operands; the test is evaluated in log2
 // units, (tile_max - running_max) * scale * log2(e) < log2(lambda), which is the
@@ -48,17 +51,24 @@ using namespace ptx;
 
 constexpr int kTile = 128;      // query rows per query tile == keys per key tile
 constexpr int kHeadDim = 128;   // d
-constexpr int kSoftmaxWarps = 4;
+constexpr int kQTiles = 2;      // query tiles per CTA
+constexpr int kSoftmaxWarps = 4;             // per query tile
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kMmaWarp = kQTiles * kSoftmaxWarps;   // 8
+constexpr int kLoadWarp = kMmaWarp + 1;             // 9
+constexpr int kThreads = 3 * 128;                   // 384: two softmax warpgroups + one for MMA / TMA
+// Register budget: 384 threads launch with 168 registers each (64512 in all); the two softmax
+// warpgroups grow to 224 and the MMA / TMA warpgroup shrinks to 56:
+// 2 x 128 x 224 + 128 x 56 = 64512.
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kControlRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // one bf16 128 x 128 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;        // 128 rows x 64 features (128-B rows)
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int buf) { return static_cast<uint32_t>(buf) * 128u; }  // S0, S1
-constexpr uint32_t kColO = 256;
+__host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 128u; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // a single wait may last at most 2 s
@@ -73,7 +83,7 @@ constexpr uint32_t kErrDrain = 1u << 3;
 __device__ uint32_t g_error_word;
 
 struct alignas(1024) Smem {
-  uint8_t q[kTileBytes];
+  uint8_t q[kQTiles][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full;
@@ -81,14 +91,15 @@ struct alignas(1024) Smem {
   uint64_t k_empty[kStages];
   uint64_t v_full[kStages];
   uint64_t v_empty[kStages];
-  uint64_t s_full[2];   // S_j in TMEM buffer j % 2 is ready (tcgen05.commit)
-  uint64_t p_ready[2];  // softmax done with buffer j % 2: decision taken, P written, O rescaled
-  uint64_t o_done;      // the last issued P V has completed
-  uint64_t drain;       // all MMAs of the CTA have completed
+  uint64_t s_full[kQTiles];   // S of tile t is ready in TMEM (tcgen05.commit)
+  uint64_t dec[kQTiles][2];   // tile t has decided key tile j (slot j % 2); flag in skip_flag
+  uint64_t p_ready[kQTiles];  // softmax t is done with S: decision taken, P written, O rescaled
+  uint64_t o_done[kQTiles];   // the last issued P V of tile t has completed
+  uint64_t drain;             // all MMAs of the CTA have completed
   uint32_t tmem_base;
-  uint32_t skip_flag[2];
-  uint32_t quit[2];     // softmax warps leave the loop together (one slot per iteration parity)
-  uint32_t abort;       // some role gave up waiting
+  uint32_t skip_flag[kQTiles][2];  // decision of tile t on key tile j, slot j % 2
+  uint32_t quit[kQTiles][2];  // softmax t leaves the loop together (one slot per iteration parity)
+  uint32_t abort;             // some role gave up waiting
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base to 1024 B
 
@@ -102,9 +113,9 @@ struct FwdParams {
   uint8_t* skip_mask;
 };
 
-// Bounded wait on an mbarrier phase. Gives up after kWaitTimeoutNs, or at once
-// when another role has given up (unless `respect_abort` is false); on a
-// timeout it records `site` in the device error word and raises the CTA abort flag.
+// Bounded wait on an mbarrier phase. Gives up after `timeout_ns`, or at once when
+// another role has given up (unless `respect_abort` is false); on a timeout it
+// records `site` in the device error word and raises the CTA abort flag.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                          uint32_t site, bool respect_abort = true,
                                          uint64_t timeout_ns = kWaitTimeoutNs) {
@@ -133,42 +144,72 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ------------------------------------------------------------------ producer
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
                                              const CUtensorMap* tv, const FwdParams& p, int b, int h,
-                                             int qt) {
+                                             int qt0) {
   volatile uint32_t* abort = &sm.abort;
   prefetch_tmap(tq);
   prefetch_tmap(tk);
   prefetch_tmap(tv);
   const uint32_t q_full = smem_u32(&sm.q_full);
-  const uint32_t qs = smem_u32(sm.q);
-  mbar_arrive_expect_tx(q_full, kTileBytes);
-  tma_load_4d(qs, tq, q_full, 0, h, qt * kTile, b);
-  tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, qt * kTile, b);
+  mbar_arrive_expect_tx(q_full, kQTiles * kTileBytes);
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    const uint32_t qs = smem_u32(sm.q[t]);
+    tma_load_4d(qs, tq, q_full, 0, h, (qt0 + t) * kTile, b);
+    tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, (qt0 + t) * kTile, b);
+  }
 
-  int k_issued[kStages] = {0, 0};  // copies issued per stage
-  int v_issued[kStages] = {0, 0};
-  for (int j = 0; j < p.nK; ++j) {
-    const int st = j & 1;
-    const uint32_t empty_parity = ((j >> 1) + 1) & 1;  // completion j/2 - 1 of the empty barrier
-    if (j >= kStages && !wait_bar(smem_u32(&sm.k_empty[st]), empty_parity, abort, kErrProducer)) break;
+  int k_issued = 0, v_issued = 0;  // copies issued; copy n goes to stage n % 2
+  auto issue_k = [&](int j) -> bool {
+    const int st = k_issued & 1;
+    if (k_issued >= kStages &&
+        !wait_bar(smem_u32(&sm.k_empty[st]), ((k_issued >> 1) + 1) & 1, abort, kErrProducer))
+      return false;
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
     mbar_arrive_expect_tx(kf, kTileBytes);
     tma_load_4d(ks, tk, kf, 0, h, j * kTile, b);
     tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, j * kTile, b);
-    ++k_issued[st];
-    if (j >= kStages && !wait_bar(smem_u32(&sm.v_empty[st]), empty_parity, abort, kErrProducer)) break;
+    ++k_issued;
+    return true;
+  };
+  auto issue_v = [&](int j) -> bool {
+    const int st = v_issued & 1;
+    if (v_issued >= kStages &&
+        !wait_bar(smem_u32(&sm.v_empty[st]), ((v_issued >> 1) + 1) & 1, abort, kErrProducer))
+      return false;
     const uint32_t vf = smem_u32(&sm.v_full[st]);
     const uint32_t vs = smem_u32(sm.v[st]);
     mbar_arrive_expect_tx(vf, kTileBytes);
     tma_load_4d(vs, tv, vf, 0, h, j * kTile, b);
     tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, j * kTile, b);
-    ++v_issued[st];
+    ++v_issued;
+    return true;
+  };
+  bool ok = issue_k(0);
+  for (int j = 0; j < p.nK && ok; ++j) {
+    if (j + 1 < p.nK && !issue_k(j + 1)) break;
+    // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
+    // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
+    // tile can decide key tile j + 1 at most before this wait, never j + 2).
+    bool loaded = false;
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, abort, kErrProducer)) { ok = false; break; }
+      const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
+      if (!skip && !loaded) {
+        if (!issue_v(j)) { ok = false; break; }
+        loaded = true;
+      }
+    }
   }
-  // Every copy this thread issued lands before the CTA may exit (immediate on the normal
-  // path, where the consumers have already waited for all of them).
-  for (int st = 0; st < kStages; ++st) {
-    if (k_issued[st] > 0) wait_bar(smem_u32(&sm.k_full[st]), (k_issued[st] - 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
-    if (v_issued[st] > 0) wait_bar(smem_u32(&sm.v_full[st]), (v_issued[st] - 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
+  // Copy n went to stage n % 2 as that stage's (n / 2)-th use, completing phase parity (n / 2) & 1.
+#pragma unroll
+  for (int back = 1; back <= kStages; ++back) {
+    const int nk = k_issued - back, nv = v_issued - back;
+    if (nk >= 0)
+      wait_bar(smem_u32(&sm.k_full[nk & 1]), (nk >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
+    if (nv >= 0)
+      wait_bar(smem_u32(&sm.v_full[nv & 1]), (nv >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
   }
   wait_bar(q_full, 0, abort, kErrDrain, false, kDrainTimeoutNs);
 }
@@ -178,62 +219,101 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   volatile uint32_t* abort = &sm.abort;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kTile, kTile, false);     // K tile is K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
-  const uint32_t qs = smem_u32(sm.q);
 
-  // S = Q K^T: 8 steps of K = 16 features. Q and K tiles are two 64-feature halves of
+  // Descriptors of every operand tile, built once; a K step only adds (offset >> 4) to the
+  // 14-bit start-address field, which never carries out of it (all tiles lie below 256 KiB).
+  // (Stage-indexed values are selected, not indexed, so that they stay in registers.)
+  const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+  const uint64_t dq1 = smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024);
+  const uint64_t dk0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+  const uint64_t dk1 = smem_desc_sw128(smem_u32(sm.k[1]), 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), kHalfBytes, 1024);
+  const uint64_t dv1 = smem_desc_sw128(smem_u32(sm.v[1]), kHalfBytes, 1024);
+  // S_t = Q_t K^T: 8 steps of K = 16 features. Q and K tiles are two 64-feature halves of
   // 128-B swizzled rows; a step advances 32 B inside a half (SBO = 8 rows x 128 B).
-  auto issue_qk = [&](uint32_t d_tmem, uint32_t ks) {
-#pragma unroll
-    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-      mma_ss(d_tmem, smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(ks + off, 16, 1024),
-             kIdescQK, kk > 0 ? 1u : 0u);
-    }
+  auto issue_qk = [&](int t, int st) {
+    const uint64_t aq = t ? dq1 : dq0;
+    const uint64_t bk = st ? dk1 : dk0;
+    const uint32_t d = tmem + col_s(t);
+    mma_ss_off<0, 0>(d, aq, bk, kIdescQK, 0u);
+    mma_ss_off<2, 2>(d, aq, bk, kIdescQK, 1u);       // +32 B
+    mma_ss_off<4, 4>(d, aq, bk, kIdescQK, 1u);       // +64 B
+    mma_ss_off<6, 6>(d, aq, bk, kIdescQK, 1u);       // +96 B
+    mma_ss_off<1024, 1024>(d, aq, bk, kIdescQK, 1u); // second 64-feature half (+16 KiB)
+    mma_ss_off<1026, 1026>(d, aq, bk, kIdescQK, 1u);
+    mma_ss_off<1028, 1028>(d, aq, bk, kIdescQK, 1u);
+    mma_ss_off<1030, 1030>(d, aq, bk, kIdescQK, 1u);
   };
-  // O (+)= P V: 8 steps of K = 16 keys. P sits in TMEM (2 bf16 per column, 8 columns
-  // per step). V rows are keys: a step advances 16 rows = 2 KiB; the two 64-feature
-  // halves are LBO = 16 KiB apart, 8-row groups SBO = 1 KiB apart.
-  auto issue_pv = [&](uint32_t p_tmem, uint32_t vs, bool accumulate) {
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      mma_ts(tmem + kColO, p_tmem + kk * 8, smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024),
-             kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-    }
+  // O_t (+)= P_t V: 8 steps of K = 16 keys. P sits in TMEM over S_t (2 bf16 per column, 8
+  // columns per step). V rows are keys: a step advances 16 rows = 2 KiB (128 in the
+  // descriptor); the two 64-feature halves are LBO = 16 KiB apart, 8-row groups SBO = 1 KiB.
+  auto issue_pv = [&](int t, int st, bool accumulate) {
+    const uint64_t bv = st ? dv1 : dv0;
+    const uint32_t d = tmem + col_o(t);
+    const uint32_t a = tmem + col_s(t);
+    mma_ts_off<0>(d, a, bv, kIdescPV, accumulate ? 1u : 0u);
+    mma_ts_off<128>(d, a + 8, bv, kIdescPV, 1u);
+    mma_ts_off<256>(d, a + 16, bv, kIdescPV, 1u);
+    mma_ts_off<384>(d, a + 24, bv, kIdescPV, 1u);
+    mma_ts_off<512>(d, a + 32, bv, kIdescPV, 1u);
+    mma_ts_off<640>(d, a + 40, bv, kIdescPV, 1u);
+    mma_ts_off<768>(d, a + 48, bv, kIdescPV, 1u);
+    mma_ts_off<896>(d, a + 56, bv, kIdescPV, 1u);
   };
 
-  int pv_issued = 0;
+  int pv_issued0 = 0, pv_issued1 = 0;
   bool ok = wait_bar(smem_u32(&sm.q_full), 0, abort, kErrMma) &&
             wait_bar(smem_u32(&sm.k_full[0]), 0, abort, kErrMma);
   if (ok) {
     tc_fence_after();
-    issue_qk(tmem + col_s(0), smem_u32(sm.k[0]));
-    tc_commit(smem_u32(&sm.s_full[0]));
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      issue_qk(t, 0);
+      tc_commit(smem_u32(&sm.s_full[t]));
+    }
     tc_commit(smem_u32(&sm.k_empty[0]));
-    for (int j = 0; j < p.nK; ++j) {
-      if (j + 1 < p.nK) {
-        // Buffer (j+1) % 2 last held tile j-1, whose P V (if any) was issued before this
-        // point; tcgen05.mma executes in issue order, so overwriting it is safe.
-        const int st = (j + 1) & 1;
-        if (!wait_bar(smem_u32(&sm.k_full[st]), ((j + 1) >> 1) & 1, abort, kErrMma)) break;
+    int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
+    for (int j = 0; j < p.nK && ok; ++j) {
+      const int st = v_used & 1;
+      const uint32_t parity = (v_used >> 1) & 1;
+      const int nst = (j + 1) & 1;
+      const bool has_next = j + 1 < p.nK;
+      bool v_ready = false;
+      bool any_kept = false;
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        // p_ready arrives once the tile has read S_t and decided: at once for a skipped
+        // key tile, after P is written (and O rescaled) for a kept one.
+        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
         tc_fence_after();
-        issue_qk(tmem + col_s(st), smem_u32(sm.k[st]));
-        tc_commit(smem_u32(&sm.s_full[st]));
-        tc_commit(smem_u32(&sm.k_empty[st]));
+        const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
+        if (!skip) {
+          if (!v_ready) {
+            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
+            tc_fence_after();
+            v_ready = true;
+          }
+          issue_pv(t, st, (t ? pv_issued1 : pv_issued0) > 0);
+          tc_commit(smem_u32(&sm.o_done[t]));
+          if (t) ++pv_issued1; else ++pv_issued0;
+          any_kept = true;
+        }
+        if (has_next) {
+          // S_t is free: it was read before p_ready, and its P (if the tile was kept) is
+          // read by the P V just issued; tcgen05.mma executes in issue order.
+          if (t == 0) {
+            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, abort, kErrMma)) { ok = false; break; }
+            tc_fence_after();
+          }
+          issue_qk(t, nst);
+          tc_commit(smem_u32(&sm.s_full[t]));
+        }
       }
-      const int sb = j & 1;
-      const uint32_t parity = (j >> 1) & 1;
-      if (!wait_bar(smem_u32(&sm.p_ready[sb]), parity, abort, kErrMma)) break;
-      tc_fence_after();
-      const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[sb]);
-      if (!wait_bar(smem_u32(&sm.v_full[sb]), parity, abort, kErrMma)) break;
-      if (!skip) {
-        tc_fence_after();
-        issue_pv(tmem + col_s(sb), smem_u32(sm.v[sb]), pv_issued > 0);
-        tc_commit(smem_u32(&sm.o_done));
-        tc_commit(smem_u32(&sm.v_empty[sb]));
-        ++pv_issued;
-      } else {
-        mbar_arrive(smem_u32(&sm.v_empty[sb]));  // V_j was loaded but is not needed
+      if (!ok) break;
+      if (has_next) tc_commit(smem_u32(&sm.k_empty[nst]));
+      if (any_kept) {  // V_j was loaded (some tile kept key tile j): release its stage
+        tc_commit(smem_u32(&sm.v_empty[st]));
+        ++v_used;
       }
     }
   }
@@ -243,19 +323,27 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-__device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, int b,
-                                            int h, int qt) {
+// Both query tiles run this one copy of the code (t selects the tile and its named barrier
+// 1 + t), which keeps the instruction footprint of the two warpgroups shared.
+__device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, int b, int h,
+                                            int t, int qt) {
   volatile uint32_t* abort = &sm.abort;
-  volatile uint32_t* quit = sm.quit;
-  const int warp = threadIdx.x >> 5;
+  volatile uint32_t* quit = sm.quit[t];
+  const int wq = (threadIdx.x >> 5) & 3;  // warp inside the warpgroup == TMEM lane quarter
   const int lane = threadIdx.x & 31;
-  const int row = threadIdx.x;  // query row inside the tile == TMEM lane
+  const int row = wq * 32 + lane;         // query row inside the tile == TMEM lane
   const int q_row = qt * kTile + row;
+  const bool tile_exists = qt < p.nQ;
   const bool row_valid = q_row < p.Sq;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t t_o = tmem + lane_base + kColO;
+  const bool leader = row == 0;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t t_s = tmem + lane_base + col_s(t);
+  const uint32_t t_o = tmem + lane_base + col_o(t);
+  const uint32_t s_full = smem_u32(&sm.s_full[t]);
+  const uint32_t p_ready = smem_u32(&sm.p_ready[t]);
+  const uint32_t o_done = smem_u32(&sm.o_done[t]);
   const size_t mask_base =
-      p.skip_mask ? ((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) : 0;
+      (p.skip_mask && tile_exists) ? ((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) : 0;
 
   float m_run = -INFINITY;  // running max of scaled scores (log2 units), kept tiles only
   float m_use = -INFINITY;  // exponent reference of l and O (trails m_run by <= 8)
@@ -266,59 +354,52 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   bool left_early = false;
 
   for (int j = 0; j < p.nK; ++j) {
-    const int sb = j & 1;
-    const uint32_t t_s = tmem + lane_base + col_s(sb);
     bool pass = true;
-    float s[kTile];
+    uint32_t sr[kTile];
     float tm2 = 0.f;
     if (!failed) {
-      const bool ok = wait_bar(smem_u32(&sm.s_full[sb]), (j >> 1) & 1, abort, kErrSoftmax);
+      const bool ok = wait_bar(s_full, j & 1, abort, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
     }
     if (!failed) {
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c * 32, r);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(r[t]);
-      }
+      tmem_ld128(t_s, sr);
       const int valid_keys = p.Sk - j * kTile;
       if (valid_keys < kTile) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
-          if (c >= valid_keys) s[c] = -INFINITY;
+          if (c >= valid_keys) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 4; c < kTile; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 0; c < kTile; c += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
       }
-      tm2 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+      mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+      tm2 = mx0 * p.scale_log2;
       // The skip test for this row; rows past Sq do not exist and always pass.
       pass = !row_valid || (tm2 - m_run < p.log2_lambda);
     } else {
-      quit[sb] = 1u;
+      quit[j & 1] = 1u;
     }
-    const bool skip = bar_and<1, kSoftmaxThreads>(pass);
-    if (quit[sb]) {  // written only before this barrier: every softmax thread sees the same value
+    const bool skip = bar_and<kSoftmaxThreads>(1u + static_cast<uint32_t>(t), pass);
+    if (quit[j & 1]) {
       left_early = true;
       break;
     }
-    if (threadIdx.x == 0 && p.skip_mask) p.skip_mask[mask_base + j] = skip ? 1 : 0;
-
+    if (leader) {
+      sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
+      mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
+      if (tile_exists && p.skip_mask) p.skip_mask[mask_base + j] = skip ? 1 : 0;
+    }
     if (skip) {
-      if (threadIdx.x == 0) {
-        sm.skip_flag[sb] = 1u;
-        ++skipped;
-      }
+      if (leader) ++skipped;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready[sb]));
+      if (lane == 0) mbar_arrive(p_ready);
       continue;
     }
 
@@ -330,59 +411,69 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       alpha = ex2_approx(m_use - m_new);  // 0 for the first kept tile
       m_use = m_new;
     }
-    const float neg_ref = -m_use;
-    // P (bf16, keys 2c and 2c+1 in column c) overwrites the first 64 columns of S_j,
-    // written in two halves of 32 columns as it is produced.
-    float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+    // P = exp2(s * scale * log2 e - m_use), two columns per packed f32x2 FMA. P (bf16, keys
+    // 2c and 2c+1 in column c) overwrites the first 64 columns of S_j, written in two halves
+    // of 32 columns as it is produced.
+    const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
+    const uint64_t nref2 = pack_f32x2(-m_use, -m_use);
+    uint64_t sum_a = pack_f32x2(0.f, 0.f), sum_b = sum_a;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
+      for (int c = 0; c < 32; ++c) {
         const int k0 = half * 64 + 2 * c;
-        const float p0 = ex2_approx(fmaf(s[k0 + 0], p.scale_log2, neg_ref));
-        const float p1 = ex2_approx(fmaf(s[k0 + 1], p.scale_log2, neg_ref));
-        const float p2 = ex2_approx(fmaf(s[k0 + 2], p.scale_log2, neg_ref));
-        const float p3 = ex2_approx(fmaf(s[k0 + 3], p.scale_log2, neg_ref));
-        sum0 += p0;
-        sum1 += p1;
-        sum2 += p2;
-        sum3 += p3;
+        const uint64_t x2 = fma_f32x2(pack_f32x2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+                                      scale2, nref2);
+        float x0, x1;
+        unpack_f32x2(x2, x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (c & 1)
+          sum_b = add_f32x2(sum_b, pack_f32x2(p0, p1));
+        else
+          sum_a = add_f32x2(sum_a, pack_f32x2(p0, p1));
         pk[c] = pack_bf16(p0, p1);
-        pk[c + 1] = pack_bf16(p2, p3);
       }
       tmem_st32(t_s + half * 32, pk);
     }
     tmem_st_wait();
-    l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
-    if (pv_count > 0) {
-      // The previous P V must be finished before O is touched (and before the next is issued).
-      const bool ok = wait_bar(smem_u32(&sm.o_done), (pv_count - 1) & 1, abort, kErrSoftmax);
+    {
+      float a0, a1, b0, b1;
+      unpack_f32x2(sum_a, a0, a1);
+      unpack_f32x2(sum_b, b0, b1);
+      l = l * alpha + ((a0 + a1) + (b0 + b1));
+    }
+    // O is rescaled only by warps that need it, after the previous P V has finished. The
+    // o_done count is then pv_count or pv_count - 1, never further off, whichever waits this
+    // thread skipped: the next P V needs this tile's p_ready, and S_j (already read) was
+    // committed after every earlier P V. So a parity wait cannot alias.
+    if (pv_count > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      const bool ok = wait_bar(o_done, (pv_count - 1) & 1, abort, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
-      if (!failed && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (!failed) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kHeadDim / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(t_o + c * 32, r);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
           tmem_st32(t_o + c * 32, r);
         }
         tmem_st_wait();
       }
     }
     if (!failed) {
-      if (threadIdx.x == 0) sm.skip_flag[sb] = 0u;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready[sb]));
+      if (lane == 0) mbar_arrive(p_ready);
     }
     ++pv_count;
   }
 
-  if (!left_early && !failed && pv_count > 0) {
-    const bool ok = wait_bar(smem_u32(&sm.o_done), (pv_count - 1) & 1, abort, kErrSoftmax);
+  if (!left_early && !failed && pv_count > 0 && tile_exists) {
+    const bool ok = wait_bar(o_done, (pv_count - 1) & 1, abort, kErrSoftmax);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -395,13 +486,13 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
         if (row_valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
+          for (int i = 0; i < 4; ++i) {
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[8 * t + 0]) * inv_l, __uint_as_float(r[8 * t + 1]) * inv_l);
-            w.y = pack_bf16(__uint_as_float(r[8 * t + 2]) * inv_l, __uint_as_float(r[8 * t + 3]) * inv_l);
-            w.z = pack_bf16(__uint_as_float(r[8 * t + 4]) * inv_l, __uint_as_float(r[8 * t + 5]) * inv_l);
-            w.w = pack_bf16(__uint_as_float(r[8 * t + 6]) * inv_l, __uint_as_float(r[8 * t + 7]) * inv_l);
-            dst[t] = w;
+            w.x = pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+            w.y = pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+            w.z = pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+            w.w = pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+            dst[i] = w;
           }
         }
       }
@@ -409,7 +500,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
         p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + q_row] = (m_use + log2f(l)) * kLn2;
     }
   }
-  if (threadIdx.x == 0 && p.skip_counts && skipped)
+  if (leader && tile_exists && p.skip_counts && skipped)
     atomicAdd(&p.skip_counts[static_cast<size_t>(b) * p.H + h], skipped);
 }
 
@@ -422,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qt0 = blockIdx.x * kQTiles, h = blockIdx.y, b = blockIdx.z;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
@@ -432,13 +523,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.v_full[s]), 1);
       mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sm.s_full[i]), 1);
-      mbar_init(smem_u32(&sm.p_ready[i]), kSoftmaxWarps);
-      sm.skip_flag[i] = 0u;
-      sm.quit[i] = 0u;
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.dec[t][0]), 1);
+      mbar_init(smem_u32(&sm.dec[t][1]), 1);
+      mbar_init(smem_u32(&sm.p_ready[t]), kSoftmaxWarps);
+      mbar_init(smem_u32(&sm.o_done[t]), 1);
+      sm.skip_flag[t][0] = 0u;
+      sm.skip_flag[t][1] = 0u;
+      sm.quit[t][0] = 0u;
+      sm.quit[t][1] = 0u;
     }
-    mbar_init(smem_u32(&sm.o_done), 1);
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0u;
     fence_mbar_init();
@@ -452,14 +547,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == kLoadWarp) {
-    if (lane == 0) run_producer(sm, &tmap_q, &tmap_k, &tmap_v, p, b, h, qt);
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma(sm, tmem, p);
-    __syncwarp();
+  if (warp >= kMmaWarp) {
+    regs_decrease<kControlRegs>();
+    if (warp == kLoadWarp) {
+      if (lane == 0) run_producer(sm, &tmap_q, &tmap_k, &tmap_v, p, b, h, qt0);
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) run_mma(sm, tmem, p);
+      __syncwarp();
+    }
   } else {
-    run_softmax(sm, tmem, p, b, h, qt);
+    regs_increase<kSoftmaxRegs>();
+    const int t = warp / kSoftmaxWarps;
+    run_softmax(sm, tmem, p, b, h, t, qt0 + t);
   }
 
   tc_fence_before();
@@ -576,7 +676,7 @@ extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const voi
   p.H = H;
   p.Sq = Sq;
   p.Sk = Sk;
-  p.nQ = (Sq + kTile - 1) / kTile;
+  p.nQ = (Sq + kTile - 1) / kTile;  // query tiles; CTAs hold kQTiles each
   p.nK = (Sk + kTile - 1) / kTile;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.log2_lambda = factor > 0.f ? static_cast<float>(std::log2(static_cast<double>(factor) / Sk))
@@ -594,7 +694,7 @@ extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const voi
   }
   void* args[] = {&tq, &tk, &tv, &p};
   const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(blasst_fwd_sm103a),
-                                         dim3(p.nQ, H, B), dim3(kThreads), args, kSmemBytes, st);
+                                         dim3((p.nQ + kQTiles - 1) / kQTiles, H, B), dim3(kThreads), args, kSmemBytes, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return BLASST_ERR_LAUNCH;
