@@ -386,11 +386,13 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       quit[j & 1] = 1u;
     }
     const bool skip = bar_and<kSoftmaxThreads>(1u + static_cast<uint32_t>(t), pass);
-    if (quit[j & 1]) {
+    if (quit[j & 1]) {  // written only before this barrier: the whole warpgroup sees one value
       left_early = true;
       break;
     }
     if (leader) {
+      // Publish the decision: the producer loads V_j only if some tile keeps key tile j,
+      // and the MMA issues P V only for a kept tile.
       sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
       mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
       if (tile_exists && p.skip_mask) p.skip_mask[mask_base + j] = skip ? 1 : 0;
