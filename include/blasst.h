@@ -90,6 +90,40 @@ const char *blasst_status_string(blasst_status s);
  */
 blasst_status blasst_device_error(uint32_t *word, int clear);
 
+/*
+ * Host-side controls (no CUDA call). They turn user settings into the factor the kernel
+ * takes, following the "Skip-Softmax" design doc (vLLM-Omni), sections "From
+ * configuration to the kernel threshold", "Timestep gating" and "Mapping the cutoff to
+ * denoising steps". Every output pointer is a host pointer owned by the caller; on
+ * BLASST_ERR_INVALID_ARG nothing is written.
+ */
+
+/* Direct control: *factor = threshold * max_kv_len, so lambda = factor / max_kv_len is the
+ * threshold itself at any sequence length. threshold finite and >= 0; max_kv_len >= 1. */
+blasst_status blasst_factor_from_threshold(double threshold, int64_t max_kv_len, double *factor);
+
+/* Calibrated control: *factor = a * exp(b * target_sparsity), a point on the curve fitted per
+ * model. Rejected unless the result is finite and >= 0. */
+blasst_status blasst_factor_from_target_sparsity(double a, double b, double target_sparsity,
+                                                 double *factor);
+
+/* Timestep gate for one attention call. disabled_until_timestep == 0 switches the gate off
+ * (t is not read; *out = factor). Otherwise *out = 0 (dense) while t > disabled_until_timestep,
+ * and also when t_published == 0, in which case *warn = 1 so that the caller can log once;
+ * once t <= disabled_until_timestep, *out = factor. warn may be NULL. factor and
+ * disabled_until_timestep finite and >= 0; t finite when published. */
+blasst_status blasst_gate_factor(double factor, double disabled_until_timestep, int t_published,
+                                 double t, double *out, int *warn);
+
+/* *dense_steps = count(t[i] > disabled_until_timestep) for i < n (t: host array of n values). */
+blasst_status blasst_dense_steps(const double *t, int n, double disabled_until_timestep,
+                                 int *dense_steps);
+
+/* Flow-shifted rectified-flow schedule: t_out[i] = s u / (1 + (s - 1) u) at the num_points
+ * uniform positions u = 1 - i / (num_points - 1) (from 1 down to 0). shift > 0,
+ * num_points >= 2; t_out holds num_points values. */
+blasst_status blasst_flow_shift_schedule(double shift, int num_points, double *t_out);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 int blasst_version(void);
 

@@ -24,3 +24,4 @@ from ._binding import (  # noqa: F401
     load_library,
 )
 from .build import build as build_library  # noqa: F401
+from . import control  # noqa: F401,E402

@@ -56,6 +56,17 @@ def load_library(path: str | None = None):
     lib.blasst_device_error.argtypes = [u32p, ctypes.c_int]
     lib.blasst_version.restype = ctypes.c_int
     lib.blasst_version.argtypes = []
+    dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
+    lib.blasst_factor_from_threshold.restype = ctypes.c_int
+    lib.blasst_factor_from_threshold.argtypes = [ctypes.c_double, ctypes.c_int64, dp]
+    lib.blasst_factor_from_target_sparsity.restype = ctypes.c_int
+    lib.blasst_factor_from_target_sparsity.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double, dp]
+    lib.blasst_gate_factor.restype = ctypes.c_int
+    lib.blasst_gate_factor.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_double, dp, ip]
+    lib.blasst_dense_steps.restype = ctypes.c_int
+    lib.blasst_dense_steps.argtypes = [dp, ctypes.c_int, ctypes.c_double, ip]
+    lib.blasst_flow_shift_schedule.restype = ctypes.c_int
+    lib.blasst_flow_shift_schedule.argtypes = [ctypes.c_double, ctypes.c_int, dp]
     if path is None:
         _lib = lib
     return lib

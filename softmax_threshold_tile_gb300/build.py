@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libblasst_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["blasst_fwd.cu"]
+SOURCES = ["blasst_fwd.cu", "blasst_host.cpp"]
 HEADERS = ["sm103_ptx.cuh"]
 INCLUDE = os.path.join(ROOT, "include")
 
