@@ -76,6 +76,47 @@ blasst_status blasst_attn_fwd(const void *q, const void *k, const void *v, void 
                               struct CUstream_st *stream, uint32_t *skip_counts,
                               uint8_t *skip_mask_dbg);
 
+/*
+ * Extended call: every argument of blasst_attn_fwd plus
+ *
+ *   max_prob      [B, H, Sq] fp32 output or NULL (packed documents: [H, total_q]): per row
+ *                 the largest softmax weight, exp(m - m) / l = 1 / l with l relative to the
+ *                 row max m over the kept keys ("video-attention" blog, "max_prob = 1 / l_i,
+ *                 and why it is free": a row-peakedness signal the pass already holds).
+ *   packed documents (variable length): cu_seqlens_q and cu_seqlens_k, DEVICE arrays of
+ *                 B + 1 int32 token offsets (non-decreasing, starting at 0), turn q / o into
+ *                 [Sq, H, 128] and k / v into [Sk, H, 128] tensors of Sq / Sk tokens in all,
+ *                 holding B documents; document b attends to its own keys only. lse and
+ *                 max_prob become [H, Sq]. max_seqlen_q / max_seqlen_k are the longest
+ *                 document lengths and max_seqlen_k is the KV length lambda is normalised by
+ *                 (lambda = factor / max_seqlen_k for every document, the design doc's
+ *                 max_kv_len, so that a threshold keeps its meaning in mixed batches).
+ *                 skip_mask_dbg must be NULL; skip_counts is [B * H]. Offsets that are out of
+ *                 order, out of the tensors or longer than the stated maxima are clamped and
+ *                 raise an error bit that blasst_device_error reports.
+ *   min_seq_len   documents (or batch entries) with fewer keys than this run dense (0 = off),
+ *                 the per-document dense fallback of packed batches.
+ *
+ * struct_size must be sizeof(blasst_fwd_args). Same return codes as blasst_attn_fwd.
+ */
+typedef struct blasst_fwd_args {
+  uint32_t struct_size;
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  float *max_prob;
+  int B, H, Sq, Sk, d;
+  float scale, factor;
+  struct CUstream_st *stream;
+  uint32_t *skip_counts;
+  uint8_t *skip_mask_dbg;
+  const int32_t *cu_seqlens_q, *cu_seqlens_k;
+  int max_seqlen_q, max_seqlen_k;
+  int min_seq_len;
+} blasst_fwd_args;
+
+blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
+
 /* A static, human-readable name for a status code. */
 const char *blasst_status_string(blasst_status s);
 

@@ -54,7 +54,7 @@ def load_library(path: str):
         u16p, u16p, u16p,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int,
-        i32p, ctypes.c_int, u8p, f64p, f64p, u8p, f64p,
+        i32p, ctypes.c_int, u8p, f64p, f64p, u8p, f64p, f64p,
     ]
     lib.oracle_dense_attn.restype = ctypes.c_int
     lib.oracle_dense_attn.argtypes = [
@@ -101,8 +101,9 @@ def skip_softmax_attn(q, k, v, scale: float, factor: float, units=None, mask_in=
     """Skip-Softmax attention on the listed (b, h, qt) units.
 
     Returns a dict with, per unit: ``o`` [n, tile_q, d] (NaN past Sq), ``lse``
-    [n, tile_q], ``mask`` [n, nK] (1 = skipped), ``gap`` [n, nK] (max over rows
-    of tile_max - running_max, natural-log units), plus ``units`` and ``nK``.
+    [n, tile_q], ``max_prob`` [n, tile_q] (1 / l), ``mask`` [n, nK] (1 = skipped),
+    ``gap`` [n, nK] (max over rows of tile_max - running_max, natural-log units),
+    plus ``units`` and ``nK``.
     ``mask_in`` [n, nK] replays given decisions instead of running the test.
     """
     lib = _load()
@@ -116,6 +117,7 @@ def skip_softmax_attn(q, k, v, scale: float, factor: float, units=None, mask_in=
     lse = np.full((n, tile_q), np.nan)
     mask = np.zeros((n, nK), dtype=np.uint8)
     gap = np.zeros((n, nK))
+    maxp = np.full((n, tile_q), np.nan)
     if mask_in is not None:
         mask_in = np.ascontiguousarray(mask_in, dtype=np.uint8).reshape(n, nK)
 
@@ -128,7 +130,8 @@ def skip_softmax_attn(q, k, v, scale: float, factor: float, units=None, mask_in=
             _ptr(units[lo:hi], ctypes.c_int32), hi - lo,
             None if mask_in is None else _ptr(mask_in[lo:hi], ctypes.c_uint8),
             _ptr(o[lo:hi], ctypes.c_double), _ptr(lse[lo:hi], ctypes.c_double),
-            _ptr(mask[lo:hi], ctypes.c_uint8), _ptr(gap[lo:hi], ctypes.c_double))
+            _ptr(mask[lo:hi], ctypes.c_uint8), _ptr(gap[lo:hi], ctypes.c_double),
+            _ptr(maxp[lo:hi], ctypes.c_double))
 
     threads = max(1, min(int(threads), n)) if n else 1
     if threads == 1:
@@ -139,7 +142,7 @@ def skip_softmax_attn(q, k, v, scale: float, factor: float, units=None, mask_in=
             rcs = list(ex.map(lambda i: run(bounds[i], bounds[i + 1]), range(threads)))
     if any(rcs):
         raise ValueError(f"oracle_skip_softmax_attn rejected its arguments (codes {rcs})")
-    return {"o": o, "lse": lse, "mask": mask, "gap": gap, "units": units, "nK": nK}
+    return {"o": o, "lse": lse, "mask": mask, "gap": gap, "max_prob": maxp, "units": units, "nK": nK}
 
 
 def dense_attn(q, k, v, scale: float, rows, threads: int = 1):

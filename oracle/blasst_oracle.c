@@ -77,6 +77,8 @@ static double dot_row(const double *x, const uint16_t *y, int d)
  *   gap    [n_units][nK]          max over rows of (tile_max - running_max);
  *                                 +inf for the first tile. The free-running
  *                                 test is gap < ln(lambda).
+ *   maxp   [n_units][tile_q]      1 / l: the row's largest softmax weight, exp(m - m) / l
+ *                                 ("video-attention" blog, "max_prob = 1 / l_i").
  * Any output pointer may be NULL.
  */
 int oracle_skip_softmax_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -84,7 +86,7 @@ int oracle_skip_softmax_attn(const uint16_t *q, const uint16_t *k, const uint16_
                              double scale, double factor, int tile_q, int tile_k,
                              const int32_t *units, int n_units,
                              const uint8_t *mask_in,
-                             double *o, double *lse, uint8_t *mask, double *gap)
+                             double *o, double *lse, uint8_t *mask, double *gap, double *maxp)
 {
     if (!q || !k || !v || !units || B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0 ||
         tile_q <= 0 || tile_k <= 0 || n_units < 0 || !(factor >= 0.0) || isinf(factor))
@@ -188,6 +190,8 @@ int oracle_skip_softmax_attn(const uint16_t *q, const uint16_t *k, const uint16_
                     o[((size_t)u * tile_q + i) * d + t] = acc[(size_t)i * d + t] / l[i];
             if (lse)
                 lse[(size_t)u * tile_q + i] = m[i] + log(l[i]);
+            if (maxp)
+                maxp[(size_t)u * tile_q + i] = 1.0 / l[i];
         }
     }
 

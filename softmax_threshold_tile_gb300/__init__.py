@@ -15,7 +15,10 @@ from ._binding import (  # noqa: F401
     TILE,
     AttnResult,
     BlasstError,
+    FwdArgs,
     attn_fwd,
+    attn_varlen_fwd,
+    blasst_attn_fwd_ex,
     blasst_attn_fwd,
     blasst_device_error,
     blasst_status_string,

@@ -25,6 +25,22 @@ HEAD_DIM = 128
 _lib = None
 
 
+class FwdArgs(ctypes.Structure):
+    """Mirror of ``blasst_fwd_args`` (include/blasst.h)."""
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("max_prob", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("Sq", ctypes.c_int), ("Sk", ctypes.c_int), ("d", ctypes.c_int),
+        ("scale", ctypes.c_float), ("factor", ctypes.c_float),
+        ("stream", ctypes.c_void_p),
+        ("skip_counts", ctypes.c_void_p), ("skip_mask_dbg", ctypes.c_void_p),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int),
+        ("min_seq_len", ctypes.c_int),
+    ]
+
+
 class BlasstError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {blasst_status_string(code)} (status {code})")
@@ -50,6 +66,8 @@ def load_library(path: str | None = None):
     lib.blasst_attn_fwd.argtypes = [vp, vp, vp, vp, f32p,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_float, ctypes.c_float, vp, vp, u8p]
+    lib.blasst_attn_fwd_ex.restype = ctypes.c_int
+    lib.blasst_attn_fwd_ex.argtypes = [ctypes.POINTER(FwdArgs)]
     lib.blasst_status_string.restype = ctypes.c_char_p
     lib.blasst_status_string.argtypes = [ctypes.c_int]
     lib.blasst_device_error.restype = ctypes.c_int
@@ -89,6 +107,22 @@ def blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream, ski
         float(scale), float(factor), _p(stream), _p(skip_counts), _p(skip_mask_dbg)))
 
 
+def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor, stream, skip_counts,
+                       skip_mask_dbg, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0,
+                       min_seq_len=0) -> int:
+    """The extended C entry point: fills a ``blasst_fwd_args`` and calls it."""
+    a = FwdArgs()
+    a.struct_size = ctypes.sizeof(FwdArgs)
+    a.q, a.k, a.v, a.o, a.lse, a.max_prob = _p(q), _p(k), _p(v), _p(o), _p(lse), _p(max_prob)
+    a.B, a.H, a.Sq, a.Sk, a.d = int(B), int(H), int(Sq), int(Sk), int(d)
+    a.scale, a.factor = float(scale), float(factor)
+    a.stream = _p(stream)
+    a.skip_counts, a.skip_mask_dbg = _p(skip_counts), _p(skip_mask_dbg)
+    a.cu_seqlens_q, a.cu_seqlens_k = _p(cu_seqlens_q), _p(cu_seqlens_k)
+    a.max_seqlen_q, a.max_seqlen_k, a.min_seq_len = int(max_seqlen_q), int(max_seqlen_k), int(min_seq_len)
+    return int(load_library().blasst_attn_fwd_ex(ctypes.byref(a)))
+
+
 def blasst_status_string(code: int) -> str:
     try:
         return load_library().blasst_status_string(int(code)).decode()
@@ -113,36 +147,85 @@ class AttnResult(NamedTuple):
     lse: object
     skip_counts: object
     skip_mask: object
+    max_prob: object = None
+
+
+def _check_qkv(q, k, v, packed: bool):
+    import torch
+    nd = 3 if packed else 4
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            shape = "[S, H, 128]" if packed else "[B, S, H, 128]"
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor {shape}")
+    if packed:
+        bad = k.shape != v.shape or k.shape[1:] != q.shape[1:]
+    else:
+        bad = k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]
+    if bad:
+        raise ValueError("q, k and v shapes disagree")
 
 
 def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, want_lse: bool = True,
-             want_counts: bool = True, want_mask: bool = False, stream=None) -> AttnResult:
+             want_counts: bool = True, want_mask: bool = False, want_max_prob: bool = False,
+             min_seq_len: int = 0, stream=None) -> AttnResult:
     """Skip-Softmax attention on torch CUDA tensors [B, S, H, 128] bf16 (contiguous).
 
-    Allocates the outputs with torch (device memory only) and calls
-    ``blasst_attn_fwd`` on the current (or given) stream. Raises BlasstError on
-    any non-OK status.
+    Allocates the outputs with torch (device memory only) and calls the C entry point on the
+    current (or given) stream. Raises BlasstError on any non-OK status.
     """
     import torch
 
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [B, S, H, 128]")
+    _check_qkv(q, k, v, packed=False)
     B, Sq, H, d = q.shape
     Sk = k.shape[1]
-    if k.shape != (B, Sk, H, d) or v.shape != k.shape:
-        raise ValueError("q [B,Sq,H,d] and k, v [B,Sk,H,d] shapes disagree")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dev = q.device
     o = out if out is not None else torch.empty_like(q)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if want_lse else None
+    mp = torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if want_max_prob else None
     counts = torch.empty((B * H,), dtype=torch.int32, device=dev) if want_counts else None
     nQ, nK = -(-Sq // TILE), -(-Sk // TILE)
     mask = torch.empty((B, H, nQ, nK), dtype=torch.uint8, device=dev) if want_mask else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    st = blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts, mask)
+    if mp is None and min_seq_len == 0:
+        st = blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts, mask)
+    else:
+        st = blasst_attn_fwd_ex(q, k, v, o, lse, mp, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts,
+                                mask, min_seq_len=min_seq_len)
     if st != BLASST_OK:
         raise BlasstError(st, "blasst_attn_fwd")
-    return AttnResult(o, lse, counts, mask)
+    return AttnResult(o, lse, counts, mask, mp)
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, factor: float,
+                    scale: float | None = None, *, out=None, want_lse: bool = True, want_counts: bool = True,
+                    want_max_prob: bool = False, min_seq_len: int = 0, stream=None) -> AttnResult:
+    """Packed documents: q / o [Tq, H, 128], k / v [Tk, H, 128] bf16 and int32 CUDA offset
+    tables of B + 1 entries. lambda = factor / max_seqlen_k for every document."""
+    import torch
+
+    _check_qkv(q, k, v, packed=True)
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or t.dim() != 1 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA int32 vector")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same B + 1 >= 2 entries")
+    Tq, H, d = q.shape
+    Tk = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=dev) if want_lse else None
+    mp = torch.empty((H, Tq), dtype=torch.float32, device=dev) if want_max_prob else None
+    counts = torch.empty((B * H,), dtype=torch.int32, device=dev) if want_counts else None
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = blasst_attn_fwd_ex(q, k, v, o, lse, mp, B, H, Tq, Tk, d, scale, factor, stream.cuda_stream, counts, None,
+                            cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, min_seq_len)
+    if st != BLASST_OK:
+        raise BlasstError(st, "blasst_attn_fwd_ex")
+    return AttnResult(o, lse, counts, None, mp)

@@ -79,6 +79,7 @@ constexpr uint32_t kErrProducer = 1u << 0;
 constexpr uint32_t kErrMma = 1u << 1;
 constexpr uint32_t kErrSoftmax = 1u << 2;
 constexpr uint32_t kErrDrain = 1u << 3;
+constexpr uint32_t kErrGeometry = 1u << 4;  // packed-document offsets out of order or too long
 
 __device__ uint32_t g_error_word;
 
@@ -104,14 +105,64 @@ struct alignas(1024) Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base to 1024 B
 
 struct FwdParams {
-  int B, H, Sq, Sk, nQ, nK;
+  int B, H, Sq, Sk, nQ, nK;  // fixed-length batch; in varlen mode Sq / Sk are the maxima
   float scale_log2;   // scale * log2(e)
   float log2_lambda;  // log2(factor / Sk); -inf when factor == 0
   __nv_bfloat16* o;
   float* lse;
+  float* max_prob;
   uint32_t* skip_counts;
   uint8_t* skip_mask;
+  const int* cu_q;    // varlen: token offsets of the B documents (B + 1 values), else null
+  const int* cu_k;
+  int Tq, Tk;         // varlen: total query / key tokens (token extents of the packed tensors)
+  int min_seq_len;    // documents with fewer keys than this run dense
 };
+
+// What one CTA works on: one batch entry (or packed document) and head, and its lengths.
+struct Geo {
+  int Sq, Sk;          // query / key length of this entry
+  int nQ, nK;          // its query / key tiles
+  int q_tok0, k_tok0;  // its first token in the token dimension of the TMA views
+  int tma_b;           // its batch coordinate in the TMA views (0 for packed documents)
+  size_t o_tok0;       // o row of its token s: (o_tok0 + s) * H + h
+  size_t stat0;        // lse / max_prob index of its token s: stat0 + s
+  float log2_lambda;
+};
+
+__device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
+  Geo g;
+  if (p.cu_q) {
+    // Offsets come from the caller's device memory: clamp them into the packed tensors so
+    // that a bad table can never address outside them, and report it.
+    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    g.q_tok0 = min(max(q0, 0), p.Tq);
+    g.k_tok0 = min(max(k0, 0), p.Tk);
+    g.Sq = min(max(q1, g.q_tok0), p.Tq) - g.q_tok0;
+    g.Sk = min(max(k1, g.k_tok0), p.Tk) - g.k_tok0;
+    if (q0 < 0 || k0 < 0 || q1 < q0 || k1 < k0 || q1 > p.Tq || k1 > p.Tk || g.Sq > p.Sq || g.Sk > p.Sk) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_error_word, kErrGeometry);
+      g.Sq = min(g.Sq, p.Sq);
+      g.Sk = min(g.Sk, p.Sk);
+    }
+    g.tma_b = 0;
+    g.o_tok0 = static_cast<size_t>(g.q_tok0);
+    g.stat0 = static_cast<size_t>(h) * p.Tq + g.q_tok0;
+  } else {
+    g.q_tok0 = 0;
+    g.k_tok0 = 0;
+    g.Sq = p.Sq;
+    g.Sk = p.Sk;
+    g.tma_b = b;
+    g.o_tok0 = static_cast<size_t>(b) * p.Sq;
+    g.stat0 = (static_cast<size_t>(b) * p.H + h) * p.Sq;
+  }
+  g.nQ = (g.Sq + kTile - 1) / kTile;
+  g.nK = (g.Sk + kTile - 1) / kTile;
+  // Short documents run dense (the per-document dense fallback of packed batches).
+  g.log2_lambda = g.Sk < p.min_seq_len ? -INFINITY : p.log2_lambda;
+  return g;
+}
 
 // Bounded wait on an mbarrier phase. Gives up after `timeout_ns`, or at once when
 // another role has given up (unless `respect_abort` is false); on a timeout it
@@ -143,8 +194,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ------------------------------------------------------------------ producer
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
-                                             const CUtensorMap* tv, const FwdParams& p, int b, int h,
-                                             int qt0) {
+                                             const CUtensorMap* tv, const Geo& g, int h, int qt0) {
   volatile uint32_t* abort = &sm.abort;
   prefetch_tmap(tq);
   prefetch_tmap(tk);
@@ -154,8 +204,8 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
     const uint32_t qs = smem_u32(sm.q[t]);
-    tma_load_4d(qs, tq, q_full, 0, h, (qt0 + t) * kTile, b);
-    tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, (qt0 + t) * kTile, b);
+    tma_load_4d(qs, tq, q_full, 0, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
+    tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
   }
 
   int k_issued = 0, v_issued = 0;  // copies issued; copy n goes to stage n % 2
@@ -167,8 +217,8 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
     mbar_arrive_expect_tx(kf, kTileBytes);
-    tma_load_4d(ks, tk, kf, 0, h, j * kTile, b);
-    tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, j * kTile, b);
+    tma_load_4d(ks, tk, kf, 0, h, g.k_tok0 + j * kTile, g.tma_b);
+    tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, g.k_tok0 + j * kTile, g.tma_b);
     ++k_issued;
     return true;
   };
@@ -180,14 +230,14 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     const uint32_t vf = smem_u32(&sm.v_full[st]);
     const uint32_t vs = smem_u32(sm.v[st]);
     mbar_arrive_expect_tx(vf, kTileBytes);
-    tma_load_4d(vs, tv, vf, 0, h, j * kTile, b);
-    tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, j * kTile, b);
+    tma_load_4d(vs, tv, vf, 0, h, g.k_tok0 + j * kTile, g.tma_b);
+    tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, g.k_tok0 + j * kTile, g.tma_b);
     ++v_issued;
     return true;
   };
   bool ok = issue_k(0);
-  for (int j = 0; j < p.nK && ok; ++j) {
-    if (j + 1 < p.nK && !issue_k(j + 1)) break;
+  for (int j = 0; j < g.nK && ok; ++j) {
+    if (j + 1 < g.nK && !issue_k(j + 1)) break;
     // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
     // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
     // tile can decide key tile j + 1 at most before this wait, never j + 2).
@@ -215,7 +265,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p) {
+__device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const Geo& g) {
   volatile uint32_t* abort = &sm.abort;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kTile, kTile, false);     // K tile is K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
@@ -273,11 +323,11 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
     }
     tc_commit(smem_u32(&sm.k_empty[0]));
     int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
-    for (int j = 0; j < p.nK && ok; ++j) {
+    for (int j = 0; j < g.nK && ok; ++j) {
       const int st = v_used & 1;
       const uint32_t parity = (v_used >> 1) & 1;
       const int nst = (j + 1) & 1;
-      const bool has_next = j + 1 < p.nK;
+      const bool has_next = j + 1 < g.nK;
       bool v_ready = false;
       bool any_kept = false;
 #pragma unroll
@@ -325,16 +375,16 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
 // ------------------------------------------------------------------ softmax + epilogue
 // Both query tiles run this one copy of the code (t selects the tile and its named barrier
 // 1 + t), which keeps the instruction footprint of the two warpgroups shared.
-__device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, int b, int h,
-                                            int t, int qt) {
+__device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
+                                            int b, int h, int t, int qt) {
   volatile uint32_t* abort = &sm.abort;
   volatile uint32_t* quit = sm.quit[t];
   const int wq = (threadIdx.x >> 5) & 3;  // warp inside the warpgroup == TMEM lane quarter
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;         // query row inside the tile == TMEM lane
   const int q_row = qt * kTile + row;
-  const bool tile_exists = qt < p.nQ;
-  const bool row_valid = q_row < p.Sq;
+  const bool tile_exists = qt < g.nQ;
+  const bool row_valid = q_row < g.Sq;
   const bool leader = row == 0;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + lane_base + col_s(t);
@@ -353,7 +403,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   bool failed = false;
   bool left_early = false;
 
-  for (int j = 0; j < p.nK; ++j) {
+  for (int j = 0; j < g.nK; ++j) {
     bool pass = true;
     uint32_t sr[kTile];
     float tm2 = 0.f;
@@ -364,7 +414,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     if (!failed) {
       tc_fence_after();
       tmem_ld128(t_s, sr);
-      const int valid_keys = p.Sk - j * kTile;
+      const int valid_keys = g.Sk - j * kTile;
       if (valid_keys < kTile) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
@@ -381,7 +431,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
       tm2 = mx0 * p.scale_log2;
       // The skip test for this row; rows past Sq do not exist and always pass.
-      pass = !row_valid || (tm2 - m_run < p.log2_lambda);
+      pass = !row_valid || (tm2 - m_run < g.log2_lambda);
     } else {
       quit[j & 1] = 1u;
     }
@@ -480,7 +530,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       tc_fence_after();
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow =
-          p.o + ((static_cast<size_t>(b) * p.Sq + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim;
+          p.o + ((g.o_tok0 + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < kHeadDim / 32; ++c) {
         uint32_t r[32];
@@ -498,8 +548,10 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
           }
         }
       }
-      if (row_valid && p.lse)
-        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + q_row] = (m_use + log2f(l)) * kLn2;
+      if (row_valid && p.lse) p.lse[g.stat0 + q_row] = (m_use + log2f(l)) * kLn2;
+      // The largest softmax weight of the row, exp(m - m) / l with l relative to the row
+      // max m ("video-attention", "max_prob = 1 / l_i"): 2^(m_run - m_use) / l here.
+      if (row_valid && p.max_prob) p.max_prob[g.stat0 + q_row] = ex2_approx(m_run - m_use) / l;
     }
   }
   if (leader && tile_exists && p.skip_counts && skipped)
@@ -516,6 +568,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int qt0 = blockIdx.x * kQTiles, h = blockIdx.y, b = blockIdx.z;
+  const Geo g = make_geo(p, b, h);
+  if (qt0 * kTile >= g.Sq) return;  // a packed document shorter than this CTA's first row
+  if (g.Sk == 0) {
+    // A document without keys: no softmax is defined; write O = 0, lse = -inf, max_prob = 0.
+    if (warp < kQTiles * kSoftmaxWarps) {
+      const int q_row = (qt0 + warp / kSoftmaxWarps) * kTile + (threadIdx.x & (kSoftmaxThreads - 1));
+      if (q_row < g.Sq) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((g.o_tok0 + q_row) * p.H + h) * kHeadDim);
+        for (int i = 0; i < kHeadDim / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse) p.lse[g.stat0 + q_row] = -INFINITY;
+        if (p.max_prob) p.max_prob[g.stat0 + q_row] = 0.f;
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
@@ -552,16 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer(sm, &tmap_q, &tmap_k, &tmap_v, p, b, h, qt0);
+      if (lane == 0) run_producer(sm, &tmap_q, &tmap_k, &tmap_v, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma(sm, tmem, p);
+      if (lane == 0) run_mma(sm, tmem, g);
       __syncwarp();
     }
   } else {
     regs_increase<kSoftmaxRegs>();
     const int t = warp / kSoftmaxWarps;
-    run_softmax(sm, tmem, p, b, h, t, qt0 + t);
+    run_softmax(sm, tmem, p, g, b, h, t, qt0 + t);
   }
 
   tc_fence_before();
@@ -647,61 +714,110 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 }  // namespace
 }  // namespace blasst
 
-extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const void* v, void* o,
-                                         float* lse, int B, int H, int Sq, int Sk, int d,
-                                         float scale, float factor, struct CUstream_st* stream,
-                                         uint32_t* skip_counts, uint8_t* skip_mask_dbg) {
-  using namespace blasst;
+namespace blasst {
+namespace {
+
+blasst_status launch(const blasst_fwd_args& a) {
+  const bool varlen = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
   // ---- argument checks: no CUDA call happens before all of them pass
-  if (!q || !k || !v || !o) return BLASST_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || B > 65535 || H > 65535) return BLASST_ERR_INVALID_ARG;
-  if (d != kHeadDim) return BLASST_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return BLASST_ERR_INVALID_ARG;
-  if (!std::isfinite(factor) || !(factor >= 0.f)) return BLASST_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+  if (!a.q || !a.k || !a.v || !a.o) return BLASST_ERR_INVALID_ARG;
+  if (a.B <= 0 || a.H <= 0 || a.Sq <= 0 || a.Sk <= 0 || a.B > 65535 || a.H > 65535) return BLASST_ERR_INVALID_ARG;
+  if (a.d != kHeadDim) return BLASST_ERR_INVALID_ARG;
+  if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return BLASST_ERR_INVALID_ARG;
+  if (!std::isfinite(a.factor) || !(a.factor >= 0.f)) return BLASST_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.o, 16))
     return BLASST_ERR_INVALID_ARG;
-  if (lse && !aligned(lse, 4)) return BLASST_ERR_INVALID_ARG;
+  if ((a.lse && !aligned(a.lse, 4)) || (a.max_prob && !aligned(a.max_prob, 4))) return BLASST_ERR_INVALID_ARG;
+  if (a.min_seq_len < 0) return BLASST_ERR_INVALID_ARG;
+  if (varlen) {
+    if (!a.cu_seqlens_q || !a.cu_seqlens_k || !aligned(a.cu_seqlens_q, 4) || !aligned(a.cu_seqlens_k, 4))
+      return BLASST_ERR_INVALID_ARG;
+    if (a.skip_mask_dbg) return BLASST_ERR_INVALID_ARG;  // the mask layout needs one length
+    if (a.max_seqlen_q <= 0 || a.max_seqlen_k <= 0 || a.max_seqlen_q > a.Sq || a.max_seqlen_k > a.Sk)
+      return BLASST_ERR_INVALID_ARG;
+  }
   // byte strides of the 4-D views must stay below 2^40 (TMA limit)
-  const double batch_stride = 256.0 * H * static_cast<double>(Sq > Sk ? Sq : Sk);
+  const double batch_stride = 256.0 * a.H * static_cast<double>(a.Sq > a.Sk ? a.Sq : a.Sk);
   if (batch_stride >= 1099511627776.0) return BLASST_ERR_INVALID_ARG;
 
   const blasst_status ds = prepare_device();
   if (ds != BLASST_OK) return ds;
 
+  // Fixed length: [B, S, H, 128] views. Packed documents: one [1, T, H, 128] view of all tokens.
+  const int tb = varlen ? 1 : a.B;
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, q, B, Sq, H) || !encode_bshd(&tk, k, B, Sk, H) ||
-      !encode_bshd(&tv, v, B, Sk, H))
+  if (!encode_bshd(&tq, a.q, tb, a.Sq, a.H) || !encode_bshd(&tk, a.k, tb, a.Sk, a.H) ||
+      !encode_bshd(&tv, a.v, tb, a.Sk, a.H))
     return BLASST_ERR_LAUNCH;
 
   FwdParams p{};
-  p.B = B;
-  p.H = H;
-  p.Sq = Sq;
-  p.Sk = Sk;
-  p.nQ = (Sq + kTile - 1) / kTile;  // query tiles; CTAs hold kQTiles each
-  p.nK = (Sk + kTile - 1) / kTile;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.log2_lambda = factor > 0.f ? static_cast<float>(std::log2(static_cast<double>(factor) / Sk))
-                               : -INFINITY;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.skip_counts = skip_counts;
-  p.skip_mask = skip_mask_dbg;
+  p.B = a.B;
+  p.H = a.H;
+  p.Sq = varlen ? a.max_seqlen_q : a.Sq;  // longest entry: sizes the grid
+  p.Sk = varlen ? a.max_seqlen_k : a.Sk;  // the KV length lambda is normalised by
+  p.nQ = (p.Sq + kTile - 1) / kTile;      // query tiles; CTAs hold kQTiles each
+  p.nK = (p.Sk + kTile - 1) / kTile;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.log2_lambda = a.factor > 0.f ? static_cast<float>(std::log2(static_cast<double>(a.factor) / p.Sk))
+                                 : -INFINITY;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.max_prob = a.max_prob;
+  p.skip_counts = a.skip_counts;
+  p.skip_mask = a.skip_mask_dbg;
+  p.cu_q = varlen ? a.cu_seqlens_q : nullptr;
+  p.cu_k = varlen ? a.cu_seqlens_k : nullptr;
+  p.Tq = a.Sq;
+  p.Tk = a.Sk;
+  p.min_seq_len = a.min_seq_len;
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (skip_counts &&
-      cudaMemsetAsync(skip_counts, 0, sizeof(uint32_t) * static_cast<size_t>(B) * H, st) != cudaSuccess) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
+  if (a.skip_counts &&
+      cudaMemsetAsync(a.skip_counts, 0, sizeof(uint32_t) * static_cast<size_t>(a.B) * a.H, st) != cudaSuccess) {
     cudaGetLastError();
     return BLASST_ERR_LAUNCH;
   }
   void* args[] = {&tq, &tk, &tv, &p};
   const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(blasst_fwd_sm103a),
-                                         dim3((p.nQ + kQTiles - 1) / kQTiles, H, B), dim3(kThreads), args, kSmemBytes, st);
+                                         dim3((p.nQ + kQTiles - 1) / kQTiles, a.H, a.B), dim3(kThreads), args,
+                                         kSmemBytes, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return BLASST_ERR_LAUNCH;
   }
   return BLASST_OK;
+}
+
+}  // namespace
+}  // namespace blasst
+
+extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const void* v, void* o,
+                                         float* lse, int B, int H, int Sq, int Sk, int d,
+                                         float scale, float factor, struct CUstream_st* stream,
+                                         uint32_t* skip_counts, uint8_t* skip_mask_dbg) {
+  blasst_fwd_args a{};
+  a.struct_size = sizeof(a);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.factor = factor;
+  a.stream = stream;
+  a.skip_counts = skip_counts;
+  a.skip_mask_dbg = skip_mask_dbg;
+  return blasst::launch(a);
+}
+
+extern "C" blasst_status blasst_attn_fwd_ex(const blasst_fwd_args* args) {
+  if (!args || args->struct_size != sizeof(blasst_fwd_args)) return BLASST_ERR_INVALID_ARG;
+  return blasst::launch(*args);
 }
 
 extern "C" const char* blasst_status_string(blasst_status s) {
@@ -710,7 +826,7 @@ extern "C" const char* blasst_status_string(blasst_status s) {
     case BLASST_ERR_INVALID_ARG: return "invalid argument";
     case BLASST_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
     case BLASST_ERR_LAUNCH: return "CUDA launch or set-up failure";
-    case BLASST_ERR_TIMEOUT: return "a device-side wait timed out";
+    case BLASST_ERR_TIMEOUT: return "a device-side wait timed out or packed-document offsets were invalid";
   }
   return "unknown status";
 }

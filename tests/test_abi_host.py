@@ -93,3 +93,42 @@ def test_package_has_no_cpu_fallback():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), fn
                 assert "softmax(" not in src, fn
+
+
+def test_extended_args_struct_matches_header(tmp_path):
+    import ctypes
+    src = tmp_path / "size.c"
+    src.write_text('#include <stdio.h>\n#include "blasst.h"\nint main(void){printf("%zu\\n", sizeof(blasst_fwd_args));return 0;}\n')
+    exe = tmp_path / "size"
+    subprocess.check_call(["gcc", "-I", INCLUDE, str(src), "-o", str(exe)])
+    size = int(subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout)
+    assert size == ctypes.sizeof(blasst.FwdArgs)
+
+
+def call_ex(**kw):
+    a = dict(q=256, k=512, v=768, o=1024, lse=None, max_prob=None, B=2, H=2, Sq=1000, Sk=1000, d=128,
+             scale=1 / math.sqrt(128), factor=2.0, stream=None, skip_counts=None, skip_mask_dbg=None,
+             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, min_seq_len=0)
+    a.update(kw)
+    return blasst.blasst_attn_fwd_ex(**a)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(cu_seqlens_q=4096),                           # only one offset table
+    dict(cu_seqlens_k=4096),
+    dict(cu_seqlens_q=4096, cu_seqlens_k=8192, max_seqlen_q=600, max_seqlen_k=600, skip_mask_dbg=64),
+    dict(cu_seqlens_q=4096, cu_seqlens_k=8192, max_seqlen_q=0, max_seqlen_k=600),
+    dict(cu_seqlens_q=4096, cu_seqlens_k=8192, max_seqlen_q=600, max_seqlen_k=1001),
+    dict(cu_seqlens_q=4098, cu_seqlens_k=8192, max_seqlen_q=600, max_seqlen_k=600),
+    dict(max_prob=1026), dict(min_seq_len=-1), dict(d=64),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_extended_invalid_arguments(lib, kw):
+    assert call_ex(**kw) == blasst.BLASST_ERR_INVALID_ARG
+
+
+def test_extended_rejects_wrong_struct_size(lib):
+    import ctypes
+    a = blasst.FwdArgs()
+    a.struct_size = ctypes.sizeof(blasst.FwdArgs) - 4
+    assert lib.blasst_attn_fwd_ex(ctypes.byref(a)) == blasst.BLASST_ERR_INVALID_ARG
+    assert lib.blasst_attn_fwd_ex(None) == blasst.BLASST_ERR_INVALID_ARG

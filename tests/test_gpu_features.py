@@ -1,0 +1,193 @@
+"""GPU tests of the extended entry point: max_prob, packed documents (variable length),
+the per-document dense fallback, and the checks on the offset tables."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import softmax_threshold_tile_gb300 as blasst
+    blasst.build_library()
+    blasst.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def _blasst():
+    import softmax_threshold_tile_gb300 as blasst
+    return blasst
+
+
+def _clear_error():
+    st, word = _blasst().blasst_device_error(clear=True)
+    return word
+
+
+@pytest.mark.parametrize("name,factor", [("tiny_1024", 0.0), ("tiny_1024", 2.0), ("dit_8192_g2", 16.0)])
+def test_max_prob_matches_oracle(name, factor):
+    import torch
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.make_qkv(w)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    res = _blasst().attn_fwd(qd, kd, vd, factor, want_mask=True, want_max_prob=True)
+    torch.cuda.synchronize()
+    assert _clear_error() == 0
+    mask = res.skip_mask.cpu().numpy()
+    mp = res.max_prob.cpu().numpy()
+    units = parity.sample_units(w.B, w.H, w.S, heads=(0, w.H - 1), qtiles=(0, 1, w.S // 256, w.S // 128 - 1))
+    m_in = np.stack([mask[b, h, t] for b, h, t in units])
+    ref = oracle.skip_softmax_attn(q, k, v, 1 / math.sqrt(w.d), factor, units=units, mask_in=m_in, threads=16)
+    for u, (b, h, t) in enumerate(units):
+        got = mp[b, h, t * 128:(t + 1) * 128]
+        np.testing.assert_allclose(got, ref["max_prob"][u], rtol=2e-3, atol=1e-6)
+    assert np.all((mp > 0) & (mp <= 1.0 + 1e-6))
+    # the plain call (no max_prob) gives bit-identical outputs
+    plain = _blasst().attn_fwd(qd, kd, vd, factor, want_mask=True)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.o, res.o) and torch.equal(plain.lse, res.lse)
+
+
+def _packed(lengths_q, lengths_k, H=3, seed=5):
+    """Packed documents: token-line clustered Q/K per document, concatenated."""
+    qs, ks, vs = [], [], []
+    for i, (lq, lk) in enumerate(zip(lengths_q, lengths_k)):
+        if lq == 0 and lk == 0:
+            continue
+        q, k, v = parity.clustered_inputs(1, H, max(lq, 1), max(lk, 1), seed=seed + i)
+        qs.append(q[0, :lq])
+        ks.append(k[0, :lk])
+        vs.append(v[0, :lk])
+    q = np.ascontiguousarray(np.concatenate(qs, 0))
+    k = np.ascontiguousarray(np.concatenate(ks, 0))
+    v = np.ascontiguousarray(np.concatenate(vs, 0))
+    cq = np.concatenate([[0], np.cumsum(lengths_q)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lengths_k)]).astype(np.int32)
+    return q, k, v, cq, ck
+
+
+def _packed_to_device(q, k, v, cq, ck):
+    import torch
+    return (parity.to_device(q), parity.to_device(k), parity.to_device(v),
+            torch.from_numpy(cq).cuda(), torch.from_numpy(ck).cuda())
+
+
+@pytest.mark.parametrize("factor", [0.0, 4.0, 64.0])
+def test_packed_documents_equal_separate_calls(factor):
+    import torch
+    lq = [1000, 37, 2048, 300, 129, 1]
+    lk = [1000, 37, 2048, 300, 129, 1]
+    q, k, v, cq, ck = _packed(lq, lk)
+    qd, kd, vd, cqd, ckd = _packed_to_device(q, k, v, cq, ck)
+    mq, mk = max(lq), max(lk)
+    res = _blasst().attn_varlen_fwd(qd, kd, vd, cqd, ckd, mq, mk, factor, want_max_prob=True)
+    torch.cuda.synchronize()
+    assert _clear_error() == 0
+    H = q.shape[1]
+    counts = res.skip_counts.cpu().numpy().reshape(len(lq), H)
+    for i, (a, b_) in enumerate(zip(lq, lk)):
+        # the same document alone, with the factor that gives the same lambda = factor / max_seqlen_k
+        fd = factor * b_ / mk
+        qi, ki, vi = (t[None, s:e].contiguous() for t, s, e in ((qd, cq[i], cq[i + 1]), (kd, ck[i], ck[i + 1]), (vd, ck[i], ck[i + 1])))
+        one = _blasst().attn_fwd(qi, ki, vi, fd, want_mask=True, want_max_prob=True)
+        torch.cuda.synchronize()
+        c1 = one.skip_counts.cpu().numpy()
+        if np.array_equal(c1, counts[i]):
+            assert torch.equal(one.o[0], res.o[cq[i]:cq[i + 1]])
+            assert torch.equal(one.lse[0], res.lse[:, cq[i]:cq[i + 1]])
+            assert torch.equal(one.max_prob[0], res.max_prob[:, cq[i]:cq[i + 1]])
+        else:
+            # lambda rounds differently through the float factor: allow only marginal tiles
+            m1 = one.skip_mask.cpu().numpy()
+            ref = oracle.skip_softmax_attn(q[None, cq[i]:cq[i + 1]].copy(), k[None, ck[i]:ck[i + 1]].copy(),
+                                           v[None, ck[i]:ck[i + 1]].copy(), 1 / math.sqrt(128), fd)
+            gap = ref["gap"].reshape(m1.shape)
+            lnlam = math.log(fd / b_) if fd > 0 else -math.inf
+            assert np.all(np.abs(gap[m1.astype(bool) != (gap < lnlam)] - lnlam) < parity.MARGIN)
+    if factor > 0:
+        assert counts.sum() > 0
+
+
+def test_packed_documents_against_oracle():
+    import torch
+    lq = [700, 1500, 260]
+    lk = [900, 1500, 130]   # cross lengths: queries and keys differ per document
+    q, k, v, cq, ck = _packed(lq, lk, H=2, seed=9)
+    qd, kd, vd, cqd, ckd = _packed_to_device(q, k, v, cq, ck)
+    factor = 8.0
+    res = _blasst().attn_varlen_fwd(qd, kd, vd, cqd, ckd, max(lq), max(lk), factor)
+    torch.cuda.synchronize()
+    assert _clear_error() == 0
+    o = res.o.float().cpu().numpy()
+    lse = res.lse.cpu().numpy()
+    for i in range(len(lq)):
+        qi, ki, vi = (np.ascontiguousarray(a[None, s:e]) for a, s, e in ((q, cq[i], cq[i + 1]), (k, ck[i], ck[i + 1]), (v, ck[i], ck[i + 1])))
+        fd = factor * lk[i] / max(lk)
+        ref = oracle.skip_softmax_attn(qi, ki, vi, 1 / math.sqrt(128), fd, threads=16)
+        for u, (_, h, t) in enumerate(ref["units"]):
+            r0, r1 = t * 128, min(lq[i], (t + 1) * 128)
+            err = np.abs(o[cq[i] + r0:cq[i] + r1, h] - ref["o"][u, :r1 - r0])
+            # free-running decisions: outputs agree to the parity bar unless a marginal tile flipped
+            assert err.max() <= parity.MAX_ABS
+            assert np.abs(lse[h, cq[i] + r0:cq[i] + r1] - ref["lse"][u, :r1 - r0]).max() <= parity.LSE_ABS
+
+
+def test_min_seq_len_runs_short_documents_dense():
+    import torch
+    lq = lk = [300, 1200, 100]
+    q, k, v, cq, ck = _packed(lq, lk, H=2, seed=21)
+    qd, kd, vd, cqd, ckd = _packed_to_device(q, k, v, cq, ck)
+    res = _blasst().attn_varlen_fwd(qd, kd, vd, cqd, ckd, 1200, 1200, 64.0, min_seq_len=301)
+    torch.cuda.synchronize()
+    counts = res.skip_counts.cpu().numpy().reshape(3, 2)
+    assert counts[0].sum() == 0 and counts[2].sum() == 0
+    for i in (0, 2):
+        qi, ki, vi = (t[None, s:e].contiguous() for t, s, e in ((qd, cq[i], cq[i + 1]), (kd, ck[i], ck[i + 1]), (vd, ck[i], ck[i + 1])))
+        dense = _blasst().attn_fwd(qi, ki, vi, 0.0)
+        torch.cuda.synchronize()
+        assert torch.equal(dense.o[0], res.o[cq[i]:cq[i + 1]])
+
+
+def test_document_without_keys_and_without_queries():
+    import torch
+    lq = [200, 0, 150, 64]
+    lk = [200, 90, 0, 64]
+    q, k, v, cq, ck = _packed(lq, lk, H=2, seed=3)
+    qd, kd, vd, cqd, ckd = _packed_to_device(q, k, v, cq, ck)
+    res = _blasst().attn_varlen_fwd(qd, kd, vd, cqd, ckd, 200, 200, 4.0, want_max_prob=True)
+    torch.cuda.synchronize()
+    assert _clear_error() == 0
+    s, e = cq[2], cq[3]  # document 2 has queries but no keys
+    assert torch.count_nonzero(res.o[s:e]) == 0
+    assert torch.all(torch.isinf(res.lse[:, s:e]) & (res.lse[:, s:e] < 0))
+    assert torch.all(res.max_prob[:, s:e] == 0)
+    assert torch.all(torch.isfinite(res.lse[:, cq[3]:cq[4]]))
+
+
+def test_bad_offset_table_is_clamped_and_reported():
+    import torch
+    lq = lk = [256, 256]
+    q, k, v, cq, ck = _packed(lq, lk, H=1, seed=4)
+    qd, kd, vd, _, _ = _packed_to_device(q, k, v, cq, ck)
+    bad_q = torch.tensor([0, 300, 200], dtype=torch.int32, device="cuda")   # out of order, past max
+    bad_k = torch.tensor([0, 256, 9999], dtype=torch.int32, device="cuda")  # past the tensor
+    _clear_error()
+    _blasst().attn_varlen_fwd(qd, kd, vd, bad_q, bad_k, 256, 256, 2.0)
+    torch.cuda.synchronize()
+    st, word = _blasst().blasst_device_error(clear=True)
+    assert word & (1 << 4)
+    # the context is still usable
+    ok = _blasst().attn_varlen_fwd(qd, kd, vd, torch.from_numpy(cq).cuda(), torch.from_numpy(ck).cuda(), 256, 256, 2.0)
+    torch.cuda.synchronize()
+    assert _clear_error() == 0
+    assert torch.isfinite(ok.o.float()).all()

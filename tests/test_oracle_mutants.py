@@ -32,6 +32,8 @@ MUTANTS = {
     "lse_log2": ("m[i] + log(l[i])", "m[i] + log2(l[i])"),
     # inverted test
     "inverted_test": ("(worst < ln_lambda)", "(worst > ln_lambda)"),
+    # max_prob as l instead of 1 / l
+    "max_prob_inverted": ("= 1.0 / l[i];", "= l[i];"),
 }
 
 
@@ -53,6 +55,7 @@ def _pin_checks():
     yield lambda: pins.test_mask_matches_prefix_max_closed_form(*pins.CLOSED_FORM_CASES[0])
     for case in pins._load_golden():
         yield lambda case=case: pins.test_hand_built_case_skips_predicted_tiles(case)
+    yield lambda: pins.test_max_prob_is_the_largest_kept_softmax_weight(20.0)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -273,3 +273,28 @@ def test_output_error_within_skipped_mass_bound(name, S, H, factors):
         n_skipped = skipped.sum(-1)
         assert np.all(delta <= lam * n_skipped + 1e-15)
     assert any_skip
+
+
+@pytest.mark.parametrize("factor", [0.0, 20.0, 100.0])
+def test_max_prob_is_the_largest_kept_softmax_weight(factor):
+    """'video-attention' blog, 'max_prob = 1 / l_i': the row's largest softmax weight."""
+    B, H, Sq, Sk, d, tq, tk = 1, 2, 70, 200, 16, 32, 32
+    rng = np.random.default_rng(12)
+    centres = rng.standard_normal((3, d)) * 4.0
+    q = synth.f32_to_bf16_bits((centres[rng.integers(0, 3, (B, Sq, H))] + rng.standard_normal((B, Sq, H, d))).astype(np.float32))
+    # keys grouped by centre along the sequence, so whole key tiles fall far below a row's max
+    k = synth.f32_to_bf16_bits((centres[(np.arange(Sk) // 40) % 3][None, :, None, :] + rng.standard_normal((B, Sk, H, d))).astype(np.float32))
+    v = random_bf16((B, Sk, H, d), 13)
+    scale = 1.0 / math.sqrt(d)
+    units = oracle.all_units(B, H, Sq, tq)
+    res = oracle.skip_softmax_attn(q, k, v, scale, factor, units=units, tile_q=tq, tile_k=tk)
+    S = scores_np(q, k, scale)[0]
+    nK = -(-Sk // tk)
+    if factor > 0:
+        assert res["mask"].sum() > 0
+    for u, (b, h, qt) in enumerate(units):
+        for i in range(min(tq, Sq - qt * tq)):
+            kept = np.concatenate([np.arange(j * tk, min(Sk, (j + 1) * tk)) for j in range(nK) if not res["mask"][u, j]])
+            s = S[h, qt * tq + i, kept]
+            w = np.exp(s - s.max())
+            assert res["max_prob"][u, i] == pytest.approx((w / w.sum()).max(), rel=1e-12)
