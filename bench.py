@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the max_prob and packed-document timings")
     ap.add_argument("--cpu-units", type=int, default=48, help="query tiles in the CPU oracle sample")
     return ap.parse_args()
 
@@ -177,15 +178,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(backend: str = "nccl"):
+    """(world, rank, local_rank) from the torchrun environment; one process per GPU."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -195,14 +198,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The largest per-rank value (the job's time is the slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes units_per_rank in its own time; the job's rate is all
+    ranks' units over the slowest rank's time (per second)."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 def cpu_oracle_rate(w, q, k, v, factor, n_units, threads):
@@ -273,7 +283,7 @@ def run_ours(args, w):
 
     import softmax_threshold_tile_gb300 as blasst
 
-    world, rank, local = dist_setup(args.gpus)
+    world, rank, local = dist_setup()
     torch.cuda.set_device(local)
     blasst.build_library()
     blasst.load_library()
@@ -325,6 +335,54 @@ def run_ours(args, w):
             s["speedup_vs_dense"] = base / s["ms"] if base else None
             s["bound"] = 1.0 / (1.0 - s["skip_fraction"] / 2.0)
 
+    # ---- the extended entry point: max_prob overhead and packed documents (not the timed region)
+    extras = None
+    if not args.no_extras and w.B == 1:
+        n_x = max(3, args.steps // 2)
+        mp = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+
+        def call_mp(f):
+            st = blasst.blasst_attn_fwd_ex(qd, kd, vd, od, lse, mp, B, H, S, S, d, scale, f, stream.cuda_stream,
+                                           counts, None)
+            if st != blasst.BLASST_OK:
+                raise blasst.BlasstError(st, "blasst_attn_fwd_ex")
+
+        for _ in range(args.warmup):
+            call_mp(head_factor)
+        ms_mp = time_calls(blasst, stream, lambda: call_mp(head_factor), n_x)
+        ms_plain = time_calls(blasst, stream, lambda: call(head_factor), n_x)
+        # Packed documents: the same tokens cut into documents of decreasing length, each
+        # attending to itself (lambda = factor / longest document).
+        lens = [S // 2]
+        while sum(lens) + lens[-1] // 2 < S and lens[-1] >= 2048:
+            lens.append(lens[-1] // 2)
+        lens.append(S - sum(lens))
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+        q3, k3, v3, o3 = (t.view(S, H, d) for t in (qd, kd, vd, od))
+        lse3 = torch.empty((H, S), dtype=torch.float32, device="cuda")
+        cnt3 = torch.empty((len(lens) * H,), dtype=torch.int32, device="cuda")
+
+        def call_varlen(f):
+            st = blasst.blasst_attn_fwd_ex(q3, k3, v3, o3, lse3, None, len(lens), H, S, S, d, scale, f,
+                                           stream.cuda_stream, cnt3, None, cu, cu, max(lens), max(lens))
+            if st != blasst.BLASST_OK:
+                raise blasst.BlasstError(st, "blasst_attn_fwd_ex")
+
+        vl = {"doc_lengths": lens}
+        packed_dense = 4.0 * H * d * sum(L * L for L in lens)
+        for f in (0.0, head_factor):
+            for _ in range(args.warmup):
+                call_varlen(f)
+            ms_v = time_calls(blasst, stream, lambda: call_varlen(f), n_x)
+            stream.synchronize()
+            skipped = int(cnt3.sum().item())
+            pairs = sum((-(-L // TILE)) ** 2 for L in lens) * H
+            vl[f"factor_{f:g}"] = {"ms": ms_v, "dense_equiv_tflops": packed_dense / ms_v / 1e9,
+                                   "skip_fraction": skipped / pairs}
+        extras = {"max_prob": {"ms_with": ms_mp, "ms_without": ms_plain, "overhead": ms_mp / ms_plain - 1.0,
+                               "factor": head_factor},
+                  "varlen": vl}
+
     # ---- the timed region: K calls at the headline factor
     m = mask_of(head_factor)
     skip = float(m.mean())
@@ -346,7 +404,7 @@ def run_ours(args, w):
     barrier(world)
     ms_local = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms_local, world)
-    value = world * dense / (ms * 1e-3) / 1e12
+    value = job_throughput(dense, world, ms) / 1e12
     achieved = ex / (ms_local * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
@@ -375,7 +433,8 @@ def run_ours(args, w):
             e2e_step()
         stream.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-        e2e = {"value": world * dense / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": job_throughput(dense, world, e2e_ms) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                "steps": n_e2e,
                "h2d_bytes_per_step": int(3 * q.nbytes),
                "d2h_bytes_per_step": int(oh.numel() * 2 + lh.numel() * 4 + ch.numel() * 4)}
@@ -409,6 +468,7 @@ def run_ours(args, w):
             "gpu_launches": args.steps,
             "clocks": clocks.summary(),
             "sweep": sweep,
+            "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -125,14 +125,39 @@ struct Geo {
   int nQ, nK;          // its query / key tiles
   int q_tok0, k_tok0;  // its first token in the token dimension of the TMA views
   int tma_b;           // its batch coordinate in the TMA views (0 for packed documents)
-  size_t o_tok0;       // o row of its token s: (o_tok0 + s) * H + h
-  size_t stat0;        // lse / max_prob index of its token s: stat0 + s
   float log2_lambda;
 };
 
+// Output addresses of token s of the CTA's entry (computed in the epilogue, not held live):
+// o row (o_tok0 + s) * H + h, lse / max_prob index stat0 + s.
+template <bool kVarlen>
+__device__ __forceinline__ size_t out_tok0(const FwdParams& p, const Geo& g, int b) {
+  return kVarlen ? static_cast<size_t>(g.q_tok0) : static_cast<size_t>(b) * p.Sq;
+}
+template <bool kVarlen>
+__device__ __forceinline__ size_t stat_base(const FwdParams& p, const Geo& g, int b, int h) {
+  return kVarlen ? static_cast<size_t>(h) * p.Tq + g.q_tok0 : (static_cast<size_t>(b) * p.H + h) * p.Sq;
+}
+
+// The lengths and threshold the hot loops read: straight from the kernel parameters for a
+// fixed-length batch (constant-bank operands, no registers held), from the CTA's geometry
+// for packed documents.
+template <bool kVarlen>
+struct Lens {
+  const FwdParams& p;
+  const Geo& g;
+  __device__ __forceinline__ int nK() const { return kVarlen ? g.nK : p.nK; }
+  __device__ __forceinline__ int Sk() const { return kVarlen ? g.Sk : p.Sk; }
+  __device__ __forceinline__ float log2_lambda() const { return kVarlen ? g.log2_lambda : p.log2_lambda; }
+  __device__ __forceinline__ int k_tok0() const { return kVarlen ? g.k_tok0 : 0; }
+};
+
+// Fixed-length batches take every length from the kernel parameters; packed documents read
+// their offset tables.
+template <bool kVarlen>
 __device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
   Geo g;
-  if (p.cu_q) {
+  if (kVarlen) {
     // Offsets come from the caller's device memory: clamp them into the packed tensors so
     // that a bad table can never address outside them, and report it.
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
@@ -146,21 +171,23 @@ __device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
       g.Sk = min(g.Sk, p.Sk);
     }
     g.tma_b = 0;
-    g.o_tok0 = static_cast<size_t>(g.q_tok0);
-    g.stat0 = static_cast<size_t>(h) * p.Tq + g.q_tok0;
   } else {
     g.q_tok0 = 0;
     g.k_tok0 = 0;
     g.Sq = p.Sq;
     g.Sk = p.Sk;
     g.tma_b = b;
-    g.o_tok0 = static_cast<size_t>(b) * p.Sq;
-    g.stat0 = (static_cast<size_t>(b) * p.H + h) * p.Sq;
   }
-  g.nQ = (g.Sq + kTile - 1) / kTile;
-  g.nK = (g.Sk + kTile - 1) / kTile;
-  // Short documents run dense (the per-document dense fallback of packed batches).
-  g.log2_lambda = g.Sk < p.min_seq_len ? -INFINITY : p.log2_lambda;
+  if (kVarlen) {
+    g.nQ = (g.Sq + kTile - 1) / kTile;
+    g.nK = (g.Sk + kTile - 1) / kTile;
+    // Short documents run dense (the per-document dense fallback of packed batches).
+    g.log2_lambda = g.Sk < p.min_seq_len ? -INFINITY : p.log2_lambda;
+  } else {
+    g.nQ = p.nQ;
+    g.nK = p.nK;
+    g.log2_lambda = p.log2_lambda;  // the host applies min_seq_len to the one length
+  }
   return g;
 }
 
@@ -193,8 +220,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ producer
+template <bool kVarlen>
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
-                                             const CUtensorMap* tv, const Geo& g, int h, int qt0) {
+                                             const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
+                                             int qt0) {
+  const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
   prefetch_tmap(tq);
   prefetch_tmap(tk);
@@ -217,8 +247,8 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
     mbar_arrive_expect_tx(kf, kTileBytes);
-    tma_load_4d(ks, tk, kf, 0, h, g.k_tok0 + j * kTile, g.tma_b);
-    tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, g.k_tok0 + j * kTile, g.tma_b);
+    tma_load_4d(ks, tk, kf, 0, h, L.k_tok0() + j * kTile, g.tma_b);
+    tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
     ++k_issued;
     return true;
   };
@@ -230,14 +260,14 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     const uint32_t vf = smem_u32(&sm.v_full[st]);
     const uint32_t vs = smem_u32(sm.v[st]);
     mbar_arrive_expect_tx(vf, kTileBytes);
-    tma_load_4d(vs, tv, vf, 0, h, g.k_tok0 + j * kTile, g.tma_b);
-    tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, g.k_tok0 + j * kTile, g.tma_b);
+    tma_load_4d(vs, tv, vf, 0, h, L.k_tok0() + j * kTile, g.tma_b);
+    tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
     ++v_issued;
     return true;
   };
   bool ok = issue_k(0);
-  for (int j = 0; j < g.nK && ok; ++j) {
-    if (j + 1 < g.nK && !issue_k(j + 1)) break;
+  for (int j = 0; j < L.nK() && ok; ++j) {
+    if (j + 1 < L.nK() && !issue_k(j + 1)) break;
     // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
     // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
     // tile can decide key tile j + 1 at most before this wait, never j + 2).
@@ -265,7 +295,9 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const Geo& g) {
+template <bool kVarlen>
+__device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
+  const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kTile, kTile, false);     // K tile is K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
@@ -323,11 +355,11 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const Geo& g) {
     }
     tc_commit(smem_u32(&sm.k_empty[0]));
     int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
-    for (int j = 0; j < g.nK && ok; ++j) {
+    for (int j = 0; j < L.nK() && ok; ++j) {
       const int st = v_used & 1;
       const uint32_t parity = (v_used >> 1) & 1;
       const int nst = (j + 1) & 1;
-      const bool has_next = j + 1 < g.nK;
+      const bool has_next = j + 1 < L.nK();
       bool v_ready = false;
       bool any_kept = false;
 #pragma unroll
@@ -375,8 +407,10 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const Geo& g) {
 // ------------------------------------------------------------------ softmax + epilogue
 // Both query tiles run this one copy of the code (t selects the tile and its named barrier
 // 1 + t), which keeps the instruction footprint of the two warpgroups shared.
+template <bool kVarlen, bool kMaxProb>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
                                             int b, int h, int t, int qt) {
+  const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
   volatile uint32_t* quit = sm.quit[t];
   const int wq = (threadIdx.x >> 5) & 3;  // warp inside the warpgroup == TMEM lane quarter
@@ -403,7 +437,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   bool failed = false;
   bool left_early = false;
 
-  for (int j = 0; j < g.nK; ++j) {
+  for (int j = 0; j < L.nK(); ++j) {
     bool pass = true;
     uint32_t sr[kTile];
     float tm2 = 0.f;
@@ -414,7 +448,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     if (!failed) {
       tc_fence_after();
       tmem_ld128(t_s, sr);
-      const int valid_keys = g.Sk - j * kTile;
+      const int valid_keys = L.Sk() - j * kTile;
       if (valid_keys < kTile) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
@@ -431,7 +465,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
       tm2 = mx0 * p.scale_log2;
       // The skip test for this row; rows past Sq do not exist and always pass.
-      pass = !row_valid || (tm2 - m_run < g.log2_lambda);
+      pass = !row_valid || (tm2 - m_run < L.log2_lambda());
     } else {
       quit[j & 1] = 1u;
     }
@@ -530,7 +564,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       tc_fence_after();
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow =
-          p.o + ((g.o_tok0 + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim;
+          p.o + ((out_tok0<kVarlen>(p, g, b) + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < kHeadDim / 32; ++c) {
         uint32_t r[32];
@@ -548,16 +582,20 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
           }
         }
       }
-      if (row_valid && p.lse) p.lse[g.stat0 + q_row] = (m_use + log2f(l)) * kLn2;
+      const size_t stat0 = stat_base<kVarlen>(p, g, b, h);
+      if (row_valid && p.lse) p.lse[stat0 + q_row] = (m_use + log2f(l)) * kLn2;
       // The largest softmax weight of the row, exp(m - m) / l with l relative to the row
       // max m ("video-attention", "max_prob = 1 / l_i"): 2^(m_run - m_use) / l here.
-      if (row_valid && p.max_prob) p.max_prob[g.stat0 + q_row] = ex2_approx(m_run - m_use) / l;
+      if (kMaxProb && row_valid) p.max_prob[stat0 + q_row] = ex2_approx(m_run - m_use) * inv_l;
     }
   }
   if (leader && tile_exists && p.skip_counts && skipped)
     atomicAdd(&p.skip_counts[static_cast<size_t>(b) * p.H + h], skipped);
 }
 
+// One instance per feature set (packed documents, max_prob output), so that the plain
+// fixed-length instance keeps the code generation of a kernel without them.
+template <bool kVarlen, bool kMaxProb>
 __global__ void __launch_bounds__(kThreads, 1)
     blasst_fwd_sm103a(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k,
@@ -568,17 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int qt0 = blockIdx.x * kQTiles, h = blockIdx.y, b = blockIdx.z;
-  const Geo g = make_geo(p, b, h);
+  const Geo g = make_geo<kVarlen>(p, b, h);
   if (qt0 * kTile >= g.Sq) return;  // a packed document shorter than this CTA's first row
   if (g.Sk == 0) {
     // A document without keys: no softmax is defined; write O = 0, lse = -inf, max_prob = 0.
     if (warp < kQTiles * kSoftmaxWarps) {
       const int q_row = (qt0 + warp / kSoftmaxWarps) * kTile + (threadIdx.x & (kSoftmaxThreads - 1));
       if (q_row < g.Sq) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((g.o_tok0 + q_row) * p.H + h) * kHeadDim);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((out_tok0<kVarlen>(p, g, b) + q_row) * p.H + h) * kHeadDim);
         for (int i = 0; i < kHeadDim / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (p.lse) p.lse[g.stat0 + q_row] = -INFINITY;
-        if (p.max_prob) p.max_prob[g.stat0 + q_row] = 0.f;
+        if (p.lse) p.lse[stat_base<kVarlen>(p, g, b, h) + q_row] = -INFINITY;
+        if (p.max_prob) p.max_prob[stat_base<kVarlen>(p, g, b, h) + q_row] = 0.f;
       }
     }
     return;
@@ -619,16 +657,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer(sm, &tmap_q, &tmap_k, &tmap_v, g, h, qt0);
+      if (lane == 0) run_producer<kVarlen>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma(sm, tmem, g);
+      if (lane == 0) run_mma<kVarlen>(sm, tmem, p, g);
       __syncwarp();
     }
   } else {
     regs_increase<kSoftmaxRegs>();
     const int t = warp / kSoftmaxWarps;
-    run_softmax(sm, tmem, p, g, b, h, t, qt0 + t);
+    run_softmax<kVarlen, kMaxProb>(sm, tmem, p, g, b, h, t, qt0 + t);
   }
 
   tc_fence_before();
@@ -700,8 +738,15 @@ blasst_status prepare_device() {
     g_dev_state[dev] = 2;
     return BLASST_ERR_UNSUPPORTED_DEVICE;
   }
-  if (cudaFuncSetAttribute(blasst_fwd_sm103a, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess) {
+  const void* kernels[4] = {reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false>),
+                            reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true>),
+                            reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false>),
+                            reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true>)};
+  bool attr_ok = true;
+  for (const void* k : kernels)
+    attr_ok = attr_ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kSmemBytes)) == cudaSuccess;
+  if (!attr_ok) {
     cudaGetLastError();
     return BLASST_ERR_LAUNCH;
   }
@@ -760,6 +805,7 @@ blasst_status launch(const blasst_fwd_args& a) {
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.log2_lambda = a.factor > 0.f ? static_cast<float>(std::log2(static_cast<double>(a.factor) / p.Sk))
                                  : -INFINITY;
+  if (!varlen && a.Sk < a.min_seq_len) p.log2_lambda = -INFINITY;  // one length: decided here
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.max_prob = a.max_prob;
@@ -778,7 +824,12 @@ blasst_status launch(const blasst_fwd_args& a) {
     return BLASST_ERR_LAUNCH;
   }
   void* args[] = {&tq, &tk, &tv, &p};
-  const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(blasst_fwd_sm103a),
+  const void* kernel =
+      varlen ? (a.max_prob ? reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true>)
+                           : reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false>))
+             : (a.max_prob ? reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true>)
+                           : reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false>));
+  const cudaError_t e = cudaLaunchKernel(kernel,
                                          dim3((p.nQ + kQTiles - 1) / kQTiles, a.H, a.B), dim3(kThreads), args,
                                          kSmemBytes, st);
   if (e != cudaSuccess) {
