@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the max_prob and packed-document timings")
+    ap.add_argument("--no-extras", action="store_true", help="skip the max_prob, packed-document and FP8 timings")
     ap.add_argument("--cpu-units", type=int, default=48, help="query tiles in the CPU oracle sample")
     return ap.parse_args()
 
@@ -379,9 +379,34 @@ def run_ours(args, w):
             pairs = sum((-(-L // TILE)) ** 2 for L in lens) * H
             vl[f"factor_{f:g}"] = {"ms": ms_v, "dense_equiv_tflops": packed_dense / ms_v / 1e9,
                                    "skip_fraction": skipped / pairs}
+        # FP8 score product: per-tensor e4m3 q / k (quantised on the device by torch: input
+        # preparation only), v and P . V in bf16.
+        fp8 = None
+        if hasattr(torch, "float8_e4m3fn"):
+            dq = float(qd.float().abs().max()) / 448.0
+            dk = float(kd.float().abs().max()) / 448.0
+            q8 = (qd.float() / dq).to(torch.float8_e4m3fn)
+            k8 = (kd.float() / dk).to(torch.float8_e4m3fn)
+
+            def call_fp8(f):
+                st = blasst.blasst_attn_fwd_ex(q8, k8, vd, od, lse, None, B, H, S, S, d, scale, f,
+                                               stream.cuda_stream, counts, None, qk_format=blasst.BLASST_QK_E4M3,
+                                               q_descale=dq, k_descale=dk)
+                if st != blasst.BLASST_OK:
+                    raise blasst.BlasstError(st, "blasst_attn_fwd_ex")
+
+            fp8 = {}
+            for f in (0.0, head_factor):
+                for _ in range(args.warmup):
+                    call_fp8(f)
+                ms_8 = time_calls(blasst, stream, lambda: call_fp8(f), n_x)
+                stream.synchronize()
+                fp8[f"factor_{f:g}"] = {"ms": ms_8, "dense_equiv_tflops": dense / ms_8 / 1e9,
+                                        "skip_fraction": int(counts.sum().item()) / (B * H * nQ * nQ)}
+            del q8, k8
         extras = {"max_prob": {"ms_with": ms_mp, "ms_without": ms_plain, "overhead": ms_mp / ms_plain - 1.0,
                                "factor": head_factor},
-                  "varlen": vl}
+                  "varlen": vl, "fp8_qk": fp8}
 
     # ---- the timed region: K calls at the headline factor
     m = mask_of(head_factor)

@@ -96,6 +96,16 @@ blasst_status blasst_attn_fwd(const void *q, const void *k, const void *v, void 
  *                 raise an error bit that blasst_device_error reports.
  *   min_seq_len   documents (or batch entries) with fewer keys than this run dense (0 = off),
  *                 the per-document dense fallback of packed batches.
+ *   qk_format     BLASST_QK_BF16 (0): q and k are bf16 as above. BLASST_QK_E4M3 (1): q and k
+ *                 are FP8 e4m3 (OCP "e4m3fn": 1 sign, 4 exponent, 3 mantissa bits, no
+ *                 infinities), one byte per element in the same layout, 16-byte aligned; the
+ *                 score product Q . K^T runs on the FP8 tensor cores with fp32 accumulation while
+ *                 v, P . V and o stay bf16. The scores are then S = (Q_e4m3 . K_e4m3^T) * scale *
+ *                 q_descale * k_descale, with q_descale / k_descale (finite, > 0, read only in
+ *                 this mode) the factors that undo the caller's per-tensor quantisation. The
+ *                 "video-attention" blog (section "First, the hardware ceiling") notes that the
+ *                 two products cost the same and only the score product tolerates the low
+ *                 precision there; the score product is the part skipping never removes.
  *
  * struct_size must be sizeof(blasst_fwd_args). Same return codes as blasst_attn_fwd.
  */
@@ -113,7 +123,11 @@ typedef struct blasst_fwd_args {
   const int32_t *cu_seqlens_q, *cu_seqlens_k;
   int max_seqlen_q, max_seqlen_k;
   int min_seq_len;
+  int qk_format;
+  float q_descale, k_descale;
 } blasst_fwd_args;
+
+enum { BLASST_QK_BF16 = 0, BLASST_QK_E4M3 = 1 };
 
 blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
 

@@ -11,6 +11,8 @@ from ._binding import (  # noqa: F401
     BLASST_ERR_TIMEOUT,
     BLASST_ERR_UNSUPPORTED_DEVICE,
     BLASST_OK,
+    BLASST_QK_BF16,
+    BLASST_QK_E4M3,
     HEAD_DIM,
     TILE,
     AttnResult,

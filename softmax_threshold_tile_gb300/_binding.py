@@ -19,6 +19,9 @@ BLASST_ERR_UNSUPPORTED_DEVICE = 2
 BLASST_ERR_LAUNCH = 3
 BLASST_ERR_TIMEOUT = 4
 
+BLASST_QK_BF16 = 0
+BLASST_QK_E4M3 = 1
+
 TILE = 128
 HEAD_DIM = 128
 
@@ -38,6 +41,8 @@ class FwdArgs(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int),
         ("min_seq_len", ctypes.c_int),
+        ("qk_format", ctypes.c_int),
+        ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
     ]
 
 
@@ -109,7 +114,7 @@ def blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream, ski
 
 def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor, stream, skip_counts,
                        skip_mask_dbg, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0,
-                       min_seq_len=0) -> int:
+                       min_seq_len=0, qk_format=BLASST_QK_BF16, q_descale=1.0, k_descale=1.0) -> int:
     """The extended C entry point: fills a ``blasst_fwd_args`` and calls it."""
     a = FwdArgs()
     a.struct_size = ctypes.sizeof(FwdArgs)
@@ -120,6 +125,7 @@ def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor
     a.skip_counts, a.skip_mask_dbg = _p(skip_counts), _p(skip_mask_dbg)
     a.cu_seqlens_q, a.cu_seqlens_k = _p(cu_seqlens_q), _p(cu_seqlens_k)
     a.max_seqlen_q, a.max_seqlen_k, a.min_seq_len = int(max_seqlen_q), int(max_seqlen_k), int(min_seq_len)
+    a.qk_format, a.q_descale, a.k_descale = int(qk_format), float(q_descale), float(k_descale)
     return int(load_library().blasst_attn_fwd_ex(ctypes.byref(a)))
 
 
@@ -150,38 +156,46 @@ class AttnResult(NamedTuple):
     max_prob: object = None
 
 
-def _check_qkv(q, k, v, packed: bool):
+def _check_qkv(q, k, v, packed: bool) -> int:
+    """Validate the operands; returns the qk format (bf16 q / k, or e4m3 q / k with bf16 v)."""
     import torch
     nd = 3 if packed else 4
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
-            shape = "[S, H, 128]" if packed else "[B, S, H, 128]"
-            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor {shape}")
+    shape = "[S, H, 128]" if packed else "[B, S, H, 128]"
+    fp8 = getattr(torch, "float8_e4m3fn", None)
+    qk_format = BLASST_QK_E4M3 if fp8 is not None and q.dtype == fp8 else BLASST_QK_BF16
+    qk_dtype = fp8 if qk_format == BLASST_QK_E4M3 else torch.bfloat16
+    for name, t, want in (("q", q, qk_dtype), ("k", k, qk_dtype), ("v", v, torch.bfloat16)):
+        if t.dtype != want or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            kind = "bf16" if want == torch.bfloat16 else "float8_e4m3fn (like q)"
+            raise ValueError(f"{name} must be a contiguous CUDA {kind} tensor {shape}")
     if packed:
         bad = k.shape != v.shape or k.shape[1:] != q.shape[1:]
     else:
         bad = k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]
     if bad:
         raise ValueError("q, k and v shapes disagree")
+    return qk_format
 
 
 def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, want_lse: bool = True,
              want_counts: bool = True, want_mask: bool = False, want_max_prob: bool = False,
-             min_seq_len: int = 0, stream=None) -> AttnResult:
-    """Skip-Softmax attention on torch CUDA tensors [B, S, H, 128] bf16 (contiguous).
+             min_seq_len: int = 0, q_descale: float = 1.0, k_descale: float = 1.0,
+             stream=None) -> AttnResult:
+    """Skip-Softmax attention on torch CUDA tensors [B, S, H, 128] (contiguous): q / k / v bf16,
+    or q / k float8_e4m3fn with v bf16 (scores then carry q_descale * k_descale).
 
     Allocates the outputs with torch (device memory only) and calls the C entry point on the
     current (or given) stream. Raises BlasstError on any non-OK status.
     """
     import torch
 
-    _check_qkv(q, k, v, packed=False)
+    qk_format = _check_qkv(q, k, v, packed=False)
     B, Sq, H, d = q.shape
     Sk = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dev = q.device
-    o = out if out is not None else torch.empty_like(q)
+    o = out if out is not None else torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if want_lse else None
     mp = torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if want_max_prob else None
     counts = torch.empty((B * H,), dtype=torch.int32, device=dev) if want_counts else None
@@ -189,11 +203,12 @@ def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, wa
     mask = torch.empty((B, H, nQ, nK), dtype=torch.uint8, device=dev) if want_mask else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    if mp is None and min_seq_len == 0:
+    if mp is None and min_seq_len == 0 and qk_format == BLASST_QK_BF16:
         st = blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts, mask)
     else:
         st = blasst_attn_fwd_ex(q, k, v, o, lse, mp, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts,
-                                mask, min_seq_len=min_seq_len)
+                                mask, min_seq_len=min_seq_len, qk_format=qk_format, q_descale=q_descale,
+                                k_descale=k_descale)
     if st != BLASST_OK:
         raise BlasstError(st, "blasst_attn_fwd")
     return AttnResult(o, lse, counts, mask, mp)
@@ -201,12 +216,14 @@ def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, wa
 
 def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, factor: float,
                     scale: float | None = None, *, out=None, want_lse: bool = True, want_counts: bool = True,
-                    want_max_prob: bool = False, min_seq_len: int = 0, stream=None) -> AttnResult:
-    """Packed documents: q / o [Tq, H, 128], k / v [Tk, H, 128] bf16 and int32 CUDA offset
-    tables of B + 1 entries. lambda = factor / max_seqlen_k for every document."""
+                    want_max_prob: bool = False, min_seq_len: int = 0, q_descale: float = 1.0,
+                    k_descale: float = 1.0, stream=None) -> AttnResult:
+    """Packed documents: q / o [Tq, H, 128], k / v [Tk, H, 128] (bf16, or e4m3 q / k as in
+    attn_fwd) and int32 CUDA offset tables of B + 1 entries. lambda = factor / max_seqlen_k
+    for every document."""
     import torch
 
-    _check_qkv(q, k, v, packed=True)
+    qk_format = _check_qkv(q, k, v, packed=True)
     for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
         if t.dtype != torch.int32 or t.dim() != 1 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA int32 vector")
@@ -218,14 +235,15 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dev = q.device
-    o = out if out is not None else torch.empty_like(q)
+    o = out if out is not None else torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((H, Tq), dtype=torch.float32, device=dev) if want_lse else None
     mp = torch.empty((H, Tq), dtype=torch.float32, device=dev) if want_max_prob else None
     counts = torch.empty((B * H,), dtype=torch.int32, device=dev) if want_counts else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     st = blasst_attn_fwd_ex(q, k, v, o, lse, mp, B, H, Tq, Tk, d, scale, factor, stream.cuda_stream, counts, None,
-                            cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, min_seq_len)
+                            cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, min_seq_len, qk_format,
+                            q_descale, k_descale)
     if st != BLASST_OK:
         raise BlasstError(st, "blasst_attn_fwd_ex")
     return AttnResult(o, lse, counts, None, mp)

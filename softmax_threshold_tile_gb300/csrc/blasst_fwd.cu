@@ -65,6 +65,7 @@ constexpr uint32_t kControlRegs = 56;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // one bf16 128 x 128 tile
+constexpr uint32_t kTileBytesF8 = kTile * kHeadDim;    // one e4m3 128 x 128 tile (128-B rows)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;        // 128 rows x 64 features (128-B rows)
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
@@ -220,7 +221,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ producer
-template <bool kVarlen>
+template <bool kVarlen, bool kFp8>
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
                                              const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
                                              int qt0) {
@@ -230,12 +231,14 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   prefetch_tmap(tk);
   prefetch_tmap(tv);
   const uint32_t q_full = smem_u32(&sm.q_full);
-  mbar_arrive_expect_tx(q_full, kQTiles * kTileBytes);
+  // e4m3 Q / K tiles are one box of 128 rows x 128 B; bf16 tiles two boxes of 64 features.
+  constexpr uint32_t kQKBytes = kFp8 ? kTileBytesF8 : kTileBytes;
+  mbar_arrive_expect_tx(q_full, kQTiles * kQKBytes);
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
     const uint32_t qs = smem_u32(sm.q[t]);
     tma_load_4d(qs, tq, q_full, 0, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
-    tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
+    if (!kFp8) tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
   }
 
   int k_issued = 0, v_issued = 0;  // copies issued; copy n goes to stage n % 2
@@ -246,9 +249,9 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
       return false;
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
-    mbar_arrive_expect_tx(kf, kTileBytes);
+    mbar_arrive_expect_tx(kf, kQKBytes);
     tma_load_4d(ks, tk, kf, 0, h, L.k_tok0() + j * kTile, g.tma_b);
-    tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
+    if (!kFp8) tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
     ++k_issued;
     return true;
   };
@@ -295,11 +298,12 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <bool kVarlen>
+template <bool kVarlen, bool kFp8>
 __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
   const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
-  constexpr uint32_t kIdescQK = idesc_bf16_f32(kTile, kTile, false);     // K tile is K-major
+  constexpr uint32_t kIdescQK = kFp8 ? idesc_e4m3_f32(kTile, kTile)          // K tile is K-major
+                                     : idesc_bf16_f32(kTile, kTile, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
 
   // Descriptors of every operand tile, built once; a K step only adds (offset >> 4) to the
@@ -317,6 +321,14 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
     const uint64_t aq = t ? dq1 : dq0;
     const uint64_t bk = st ? dk1 : dk0;
     const uint32_t d = tmem + col_s(t);
+    if (kFp8) {
+      // e4m3: 4 steps of K = 32 features, 32 B apart inside the one 128-B swizzled row.
+      mma_ss_f8_off<0, 0>(d, aq, bk, kIdescQK, 0u);
+      mma_ss_f8_off<2, 2>(d, aq, bk, kIdescQK, 1u);
+      mma_ss_f8_off<4, 4>(d, aq, bk, kIdescQK, 1u);
+      mma_ss_f8_off<6, 6>(d, aq, bk, kIdescQK, 1u);
+      return;
+    }
     mma_ss_off<0, 0>(d, aq, bk, kIdescQK, 0u);
     mma_ss_off<2, 2>(d, aq, bk, kIdescQK, 1u);       // +32 B
     mma_ss_off<4, 4>(d, aq, bk, kIdescQK, 1u);       // +64 B
@@ -595,7 +607,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
 
 // One instance per feature set (packed documents, max_prob output), so that the plain
 // fixed-length instance keeps the code generation of a kernel without them.
-template <bool kVarlen, bool kMaxProb>
+template <bool kVarlen, bool kMaxProb, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     blasst_fwd_sm103a(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k,
@@ -657,10 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer<kVarlen>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
+      if (lane == 0) run_producer<kVarlen, kFp8>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma<kVarlen>(sm, tmem, p, g);
+      if (lane == 0) run_mma<kVarlen, kFp8>(sm, tmem, p, g);
       __syncwarp();
     }
   } else {
@@ -697,21 +709,36 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B, S, H, 128] bf16 viewed as a 4-D tensor (d, H, S, B); boxes of 64 features x 1 head x
-// 128 tokens x 1 batch, 128-byte swizzled. Tokens past S read as zero.
-bool encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H) {
+// [B, S, H, 128] viewed as a 4-D tensor (d, H, S, B); boxes of 128 bytes of features (64 bf16
+// or 128 e4m3) x 1 head x 128 tokens x 1 batch, 128-byte swizzled. Tokens past S read as zero.
+bool encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, bool e4m3 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
-  const cuuint64_t row = static_cast<cuuint64_t>(kHeadDim) * 2;
+  const cuuint64_t row = static_cast<cuuint64_t>(kHeadDim) * (e4m3 ? 1 : 2);
   const cuuint64_t strides[3] = {row, row * static_cast<cuuint64_t>(H),
                                  row * static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(S)};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t box[4] = {e4m3 ? 128u : 64u, 1, static_cast<cuuint32_t>(kTile), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+  return fn(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K).
+const void* kernel_for(int bits) {
+  switch (bits & 7) {
+    case 0: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false, false>);
+    case 1: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false, false>);
+    case 2: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true, false>);
+    case 3: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true, false>);
+    case 4: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false, true>);
+    case 5: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false, true>);
+    case 6: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true, true>);
+    default: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true, true>);
+  }
 }
 
 constexpr int kMaxDevices = 64;
@@ -738,13 +765,9 @@ blasst_status prepare_device() {
     g_dev_state[dev] = 2;
     return BLASST_ERR_UNSUPPORTED_DEVICE;
   }
-  const void* kernels[4] = {reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false>),
-                            reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true>),
-                            reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false>),
-                            reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true>)};
   bool attr_ok = true;
-  for (const void* k : kernels)
-    attr_ok = attr_ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  for (int i = 0; i < 8; ++i)
+    attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(i), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(kSmemBytes)) == cudaSuccess;
   if (!attr_ok) {
     cudaGetLastError();
@@ -770,6 +793,15 @@ blasst_status launch(const blasst_fwd_args& a) {
   if (a.d != kHeadDim) return BLASST_ERR_INVALID_ARG;
   if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return BLASST_ERR_INVALID_ARG;
   if (!std::isfinite(a.factor) || !(a.factor >= 0.f)) return BLASST_ERR_INVALID_ARG;
+  if (a.qk_format != BLASST_QK_BF16 && a.qk_format != BLASST_QK_E4M3) return BLASST_ERR_INVALID_ARG;
+  const bool e4m3 = a.qk_format == BLASST_QK_E4M3;
+  double qk_descale = 1.0;
+  if (e4m3) {
+    if (!std::isfinite(a.q_descale) || !(a.q_descale > 0.f) || !std::isfinite(a.k_descale) ||
+        !(a.k_descale > 0.f))
+      return BLASST_ERR_INVALID_ARG;
+    qk_descale = static_cast<double>(a.q_descale) * static_cast<double>(a.k_descale);
+  }
   if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.o, 16))
     return BLASST_ERR_INVALID_ARG;
   if ((a.lse && !aligned(a.lse, 4)) || (a.max_prob && !aligned(a.max_prob, 4))) return BLASST_ERR_INVALID_ARG;
@@ -791,7 +823,7 @@ blasst_status launch(const blasst_fwd_args& a) {
   // Fixed length: [B, S, H, 128] views. Packed documents: one [1, T, H, 128] view of all tokens.
   const int tb = varlen ? 1 : a.B;
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, a.q, tb, a.Sq, a.H) || !encode_bshd(&tk, a.k, tb, a.Sk, a.H) ||
+  if (!encode_bshd(&tq, a.q, tb, a.Sq, a.H, e4m3) || !encode_bshd(&tk, a.k, tb, a.Sk, a.H, e4m3) ||
       !encode_bshd(&tv, a.v, tb, a.Sk, a.H))
     return BLASST_ERR_LAUNCH;
 
@@ -802,7 +834,7 @@ blasst_status launch(const blasst_fwd_args& a) {
   p.Sk = varlen ? a.max_seqlen_k : a.Sk;  // the KV length lambda is normalised by
   p.nQ = (p.Sq + kTile - 1) / kTile;      // query tiles; CTAs hold kQTiles each
   p.nK = (p.Sk + kTile - 1) / kTile;
-  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * qk_descale * 1.4426950408889634);
   p.log2_lambda = a.factor > 0.f ? static_cast<float>(std::log2(static_cast<double>(a.factor) / p.Sk))
                                  : -INFINITY;
   if (!varlen && a.Sk < a.min_seq_len) p.log2_lambda = -INFINITY;  // one length: decided here
@@ -824,11 +856,7 @@ blasst_status launch(const blasst_fwd_args& a) {
     return BLASST_ERR_LAUNCH;
   }
   void* args[] = {&tq, &tk, &tv, &p};
-  const void* kernel =
-      varlen ? (a.max_prob ? reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true>)
-                           : reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false>))
-             : (a.max_prob ? reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true>)
-                           : reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false>));
+  const void* kernel = kernel_for((varlen ? 1 : 0) | (a.max_prob ? 2 : 0) | (e4m3 ? 4 : 0));
   const cudaError_t e = cudaLaunchKernel(kernel,
                                          dim3((p.nQ + kQTiles - 1) / kQTiles, a.H, a.B), dim3(kThreads), args,
                                          kSmemBytes, st);
@@ -904,4 +932,4 @@ extern "C" blasst_status blasst_device_error(uint32_t* word, int clear) {
   return w ? BLASST_ERR_TIMEOUT : BLASST_OK;
 }
 
-extern "C" int blasst_version(void) { return 100; }
+extern "C" int blasst_version(void) { return 10100; }

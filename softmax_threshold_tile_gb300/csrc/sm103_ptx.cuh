@@ -151,6 +151,21 @@ __device__ __forceinline__ void mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, kind::f8f6f4 (e4m3 in, fp32 accumulate), with
+// compile-time offsets added to the descriptors inside the asm block.
+template <uint32_t kOffA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ss_f8_off(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "add.u64 da, %1, %5;\n\t"
+      "add.u64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
+      : "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of this warp's 32 lanes, waited for before return.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -234,6 +249,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) |
          ((M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0) and fp32 D, both
+// operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- misc

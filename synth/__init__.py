@@ -77,6 +77,47 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+
+E4M3_MAX = 448.0  # largest finite OCP FP8 e4m3 ("e4m3fn") value: 1.75 * 2^8
+
+
+def f32_to_e4m3_bits(x) -> np.ndarray:
+    """Round float32 values to OCP FP8 e4m3 bit patterns (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; no infinities), nearest-even, saturating to +-448. Codes 0x7F / 0xFF (NaN)
+    are produced only for NaN input."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.uint8) << 7
+    a = np.minimum(np.abs(np.nan_to_num(x, nan=0.0)), E4M3_MAX)
+    _, ex = np.frexp(a)                     # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)              # unbiased exponent; below 2^-6 the subnormal step
+    q = np.rint(a / np.ldexp(1.0, e - 3))   # mantissa with the leading one, in steps of 1/8
+    # normal: code = (e + 7) * 8 + (q - 8); q == 16 carries into the exponent on its own.
+    # subnormal (e == -6, q < 8): code = q.
+    code = np.where(q >= 8, (e + 7) * 8 + (q - 8), q).astype(np.int64)
+    out = (code.astype(np.uint8) | sign).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), out).astype(np.uint8)
+
+
+def e4m3_bits_to_f32(bits) -> np.ndarray:
+    """Decode OCP FP8 e4m3 bit patterns (0x7F / 0xFF are NaN)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    e = (b >> 3) & 0xF
+    m = b & 7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    val = np.where(b & 0x80, -mag, mag)
+    val = np.where((b & 0x7F) == 0x7F, np.nan, val)
+    return val.astype(np.float32)
+
+
+def quantize_e4m3(bits_bf16):
+    """Per-tensor FP8 quantisation of a bf16 tensor, as a caller would do before an e4m3 call:
+    descale = amax / 448, codes = e4m3(x / descale). Returns (uint8 codes, descale)."""
+    x = bf16_bits_to_f32(bits_bf16).astype(np.float64)
+    amax = float(np.abs(x).max()) if x.size else 0.0
+    descale = amax / E4M3_MAX if amax > 0 else 1.0
+    descale = float(np.float32(descale))
+    return f32_to_e4m3_bits((x / descale).astype(np.float32)), descale
+
 @dataclass
 class Workload:
     """One synthetic attention problem: shapes, token grid, clustering and factor sweep."""

@@ -121,6 +121,10 @@ def call_ex(**kw):
     dict(cu_seqlens_q=4096, cu_seqlens_k=8192, max_seqlen_q=600, max_seqlen_k=1001),
     dict(cu_seqlens_q=4098, cu_seqlens_k=8192, max_seqlen_q=600, max_seqlen_k=600),
     dict(max_prob=1026), dict(min_seq_len=-1), dict(d=64),
+    dict(qk_format=2), dict(qk_format=-1),                  # unknown score-operand format
+    dict(qk_format=1, q_descale=0.0), dict(qk_format=1, k_descale=-2.0),
+    dict(qk_format=1, q_descale=float("nan")), dict(qk_format=1, k_descale=float("inf")),
+    dict(qk_format=1, q=264),                               # e4m3 q must still be 16-byte aligned
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_extended_invalid_arguments(lib, kw):
     assert call_ex(**kw) == blasst.BLASST_ERR_INVALID_ARG

@@ -2,6 +2,7 @@
 import math
 
 import numpy as np
+import pytest
 
 import synth
 
@@ -73,3 +74,53 @@ def test_workload_grids_cover_their_tokens():
         T, Hg, W = w.grid
         assert T * Hg * W == w.S, w.name
         assert math.isfinite(w.dense_flops())
+
+
+def test_e4m3_codes_follow_the_ocp_definition():
+    # hand values of the OCP FP8 e4m3 format (bias 7, 3 mantissa bits, no infinities)
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x30: 0.5, 0x3C: 1.5, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0, 0x40: 2.0}
+    for code, val in cases.items():
+        assert synth.e4m3_bits_to_f32(np.array([code], np.uint8))[0] == np.float32(val)
+        assert synth.f32_to_e4m3_bits(np.array([val], np.float32))[0] == code or val == 0.0
+    assert np.isnan(synth.e4m3_bits_to_f32(np.array([0x7F, 0xFF], np.uint8))).all()
+    # ties go to the even code; out-of-range values saturate
+    x = np.array([2.0 ** -10, 3 * 2.0 ** -10, 1.0625, 1.1875, 1000.0, -1e9, 464.0], np.float32)
+    np.testing.assert_array_equal(synth.f32_to_e4m3_bits(x), [0x00, 0x02, 0x38, 0x3A, 0x7E, 0xFE, 0x7E])
+
+
+def test_e4m3_round_trip_and_bf16_exactness():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = synth.e4m3_bits_to_f32(codes)
+    np.testing.assert_array_equal(synth.f32_to_e4m3_bits(vals)[vals != 0], codes[vals != 0])
+    # every finite e4m3 value is a bf16 value, so the oracle can take e4m3 inputs as bf16 bits
+    np.testing.assert_array_equal(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(vals)), vals)
+
+
+def test_e4m3_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = synth.e4m3_bits_to_f32(codes)
+    np.testing.assert_array_equal(np.isnan(ref), np.isnan(got))
+    np.testing.assert_array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)])
+    rng = np.random.default_rng(1)
+    fin = np.sort(ref[np.isfinite(ref)])
+    x = np.concatenate([rng.standard_normal(20000) * np.exp(rng.uniform(-12, 6, 20000)),
+                        (fin[:-1] + fin[1:]) / 2]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    np.testing.assert_array_equal(synth.f32_to_e4m3_bits(x),
+                                  torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_quantize_e4m3_per_tensor():
+    q, _, _ = synth.make_qkv("tiny_1024")
+    codes, descale = synth.quantize_e4m3(q)
+    x = synth.bf16_bits_to_f32(q)
+    assert abs(descale * 448.0 - np.abs(x).max()) <= 1e-6 * np.abs(x).max()
+    back = synth.e4m3_bits_to_f32(codes) * descale
+    # relative rounding error of e4m3 is at most 2^-4 for normal values
+    big = np.abs(x) > 2.0 ** -6 * descale
+    assert np.all(np.abs(back[big] - x[big]) <= 2.0 ** -4 * np.abs(x[big]) * (1 + 1e-6))
