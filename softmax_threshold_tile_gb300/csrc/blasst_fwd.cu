@@ -664,28 +664,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
 
+  // Nothing computed above stays live past the role branch: values that cross it would have
+  // to survive the softmax region at its register limit, and the compiler would spill them
+  // and reload them inside the MMA issue loop. The join below re-derives what it needs.
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
       if (lane == 0) run_producer<kVarlen, kFp8>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma<kVarlen, kFp8>(sm, tmem, p, g);
+      if (lane == 0) run_mma<kVarlen, kFp8>(sm, sm.tmem_base, p, g);
       __syncwarp();
     }
   } else {
     regs_increase<kSoftmaxRegs>();
     const int t = warp / kSoftmaxWarps;
-    run_softmax<kVarlen, kMaxProb>(sm, tmem, p, g, b, h, t, qt0 + t);
+    run_softmax<kVarlen, kMaxProb>(sm, sm.tmem_base, p, g, b, h, t, qt0 + t);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if ((threadIdx.x >> 5) == kMmaWarp) {
+    Smem& sm2 = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                         ~static_cast<uintptr_t>(1023));
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(&sm2.tmem_base), kTmemCols);
   }
 }
 
