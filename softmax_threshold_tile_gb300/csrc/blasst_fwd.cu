@@ -96,7 +96,7 @@ struct alignas(1024) Smem {
   uint64_t s_full[kQTiles];   // S of tile t is ready in TMEM (tcgen05.commit)
   uint64_t dec[kQTiles][2];   // tile t has decided key tile j (slot j % 2); flag in skip_flag
   uint64_t p_ready[kQTiles];  // softmax t is done with S: decision taken, P written, O rescaled
-  uint64_t o_done[kQTiles];   // the last issued P V of tile t has completed
+  uint64_t o_done[kQTiles];   // every MMA of the CTA has completed (one phase, after the loop)
   uint64_t drain;             // all MMAs of the CTA have completed
   uint32_t tmem_base;
   uint32_t skip_flag[kQTiles][2];  // decision of tile t on key tile j, slot j % 2
@@ -388,7 +388,6 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
             v_ready = true;
           }
           issue_pv(t, st, (t ? pv_issued1 : pv_issued0) > 0);
-          tc_commit(smem_u32(&sm.o_done[t]));
           if (t) ++pv_issued1; else ++pv_issued0;
           any_kept = true;
         }
@@ -411,6 +410,12 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
       }
     }
   }
+  // The softmax epilogues read O once every P V has completed. Inside the loop no such signal
+  // is needed: S_t(j + 1) is committed after the P V of key tile j, and a commit tracks every
+  // earlier MMA of this thread, so a softmax that has S_t(j + 1) knows its earlier P V are
+  // done. Committed on every exit path, so the epilogue waits never hang.
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) tc_commit(smem_u32(&sm.o_done[t]));
   // Every MMA this thread issued completes before TMEM is released.
   tc_commit(smem_u32(&sm.drain));
   wait_bar(smem_u32(&sm.drain), 0, abort, kErrDrain, false, kDrainTimeoutNs);
@@ -542,36 +547,27 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
       unpack_f32x2(sum_b, b0, b1);
       l = l * alpha + ((a0 + a1) + (b0 + b1));
     }
-    // O is rescaled only by warps that need it, after the previous P V has finished. The
-    // o_done count is then pv_count or pv_count - 1, never further off, whichever waits this
-    // thread skipped: the next P V needs this tile's p_ready, and S_j (already read) was
-    // committed after every earlier P V. So a parity wait cannot alias.
+    // O is rescaled only by warps that need it. Every earlier P V of this tile has completed:
+    // S_j, which this thread waited for, was committed after them.
     if (pv_count > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-      const bool ok = wait_bar(o_done, (pv_count - 1) & 1, abort, kErrSoftmax);
-      failed = !__all_sync(0xffffffffu, ok);
-      if (!failed) {
-        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kHeadDim / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);
+      for (int c = 0; c < kHeadDim / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(t_o + c * 32, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(t_o + c * 32, r);
-        }
-        tmem_st_wait();
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st32(t_o + c * 32, r);
       }
+      tmem_st_wait();
     }
-    if (!failed) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
-    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_ready);
     ++pv_count;
   }
 
   if (!left_early && !failed && pv_count > 0 && tile_exists) {
-    const bool ok = wait_bar(o_done, (pv_count - 1) & 1, abort, kErrSoftmax);
+    const bool ok = wait_bar(o_done, 0, abort, kErrSoftmax);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
