@@ -90,9 +90,7 @@ struct alignas(1024) Smem {
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full;
   uint64_t k_full[kStages];
-  uint64_t k_empty[kStages];
   uint64_t v_full[kStages];
-  uint64_t v_empty[kStages];
   uint64_t s_full[kQTiles];   // S of tile t is ready in TMEM (tcgen05.commit)
   uint64_t dec[kQTiles][2];   // tile t has decided key tile j (slot j % 2); flag in skip_flag
   uint64_t p_ready[kQTiles];  // softmax t is done with S: decision taken, P written, O rescaled
@@ -241,36 +239,36 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     if (!kFp8) tma_load_4d(qs + kHalfBytes, tq, q_full, 64, h, g.q_tok0 + (qt0 + t) * kTile, g.tma_b);
   }
 
-  int k_issued = 0, v_issued = 0;  // copies issued; copy n goes to stage n % 2
-  auto issue_k = [&](int j) -> bool {
+  // Copy n goes to stage n % 2, over copy n - 2. No "stage empty" barrier is needed: both
+  // tiles' decisions on key tile i are published only after their softmax has read S(i), and
+  // S_B(i) is committed after every earlier MMA of the CTA. So once this thread has waited for
+  // both decisions on key tile i, every MMA up to Q_B K_i^T has completed, which covers the
+  // readers of K_(i) and of every V tile used before key tile i. K_(j+1) is issued after the
+  // decisions on key tile j - 1 (its stage held K_(j-1)); V copy n, at key tile j, after the
+  // decisions on key tile j - 1, while copy n - 2 served a key tile at most j - 2.
+  int k_issued = 0, v_issued = 0;
+  auto issue_k = [&](int j) {
     const int st = k_issued & 1;
-    if (k_issued >= kStages &&
-        !wait_bar(smem_u32(&sm.k_empty[st]), ((k_issued >> 1) + 1) & 1, abort, kErrProducer))
-      return false;
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
     mbar_arrive_expect_tx(kf, kQKBytes);
     tma_load_4d(ks, tk, kf, 0, h, L.k_tok0() + j * kTile, g.tma_b);
     if (!kFp8) tma_load_4d(ks + kHalfBytes, tk, kf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
     ++k_issued;
-    return true;
   };
-  auto issue_v = [&](int j) -> bool {
+  auto issue_v = [&](int j) {
     const int st = v_issued & 1;
-    if (v_issued >= kStages &&
-        !wait_bar(smem_u32(&sm.v_empty[st]), ((v_issued >> 1) + 1) & 1, abort, kErrProducer))
-      return false;
     const uint32_t vf = smem_u32(&sm.v_full[st]);
     const uint32_t vs = smem_u32(sm.v[st]);
     mbar_arrive_expect_tx(vf, kTileBytes);
     tma_load_4d(vs, tv, vf, 0, h, L.k_tok0() + j * kTile, g.tma_b);
     tma_load_4d(vs + kHalfBytes, tv, vf, 64, h, L.k_tok0() + j * kTile, g.tma_b);
     ++v_issued;
-    return true;
   };
-  bool ok = issue_k(0);
+  issue_k(0);
+  bool ok = true;
   for (int j = 0; j < L.nK() && ok; ++j) {
-    if (j + 1 < L.nK() && !issue_k(j + 1)) break;
+    if (j + 1 < L.nK()) issue_k(j + 1);
     // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
     // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
     // tile can decide key tile j + 1 at most before this wait, never j + 2).
@@ -280,7 +278,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
       if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, abort, kErrProducer)) { ok = false; break; }
       const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
       if (!skip && !loaded) {
-        if (!issue_v(j)) { ok = false; break; }
+        issue_v(j);
         loaded = true;
       }
     }
@@ -365,7 +363,6 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
       issue_qk(t, 0);
       tc_commit(smem_u32(&sm.s_full[t]));
     }
-    tc_commit(smem_u32(&sm.k_empty[0]));
     int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
     for (int j = 0; j < L.nK() && ok; ++j) {
       const int st = v_used & 1;
@@ -403,11 +400,7 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
         }
       }
       if (!ok) break;
-      if (has_next) tc_commit(smem_u32(&sm.k_empty[nst]));
-      if (any_kept) {  // V_j was loaded (some tile kept key tile j): release its stage
-        tc_commit(smem_u32(&sm.v_empty[st]));
-        ++v_used;
-      }
+      if (any_kept) ++v_used;  // V_j was loaded (some tile kept key tile j)
     }
   }
   // The softmax epilogues read O once every P V has completed. Inside the loop no such signal
@@ -634,9 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
       mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(smem_u32(&sm.s_full[t]), 1);
