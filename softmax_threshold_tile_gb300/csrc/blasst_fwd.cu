@@ -98,7 +98,9 @@ struct alignas(1024) Smem {
   uint64_t drain;             // all MMAs of the CTA have completed
   uint32_t tmem_base;
   uint32_t skip_flag[kQTiles][2];  // decision of tile t on key tile j, slot j % 2
-  uint32_t quit[kQTiles][2];  // softmax t leaves the loop together (one slot per iteration parity)
+  uint32_t quit[kQTiles][2];  // the softmax warps leave the loop together (tile, step parity)
+  float hmax[kQTiles][2][kTile];   // half-row maxima of the current key tile (tile, half, row)
+  float lpart[kQTiles][2][kTile];  // half-row sums at the end (tile, half, row)
   uint32_t abort;             // some role gave up waiting
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base to 1024 B
@@ -415,112 +417,122 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-// Both query tiles run this one copy of the code (t selects the tile and its named barrier
-// 1 + t), which keeps the instruction footprint of the two warpgroups shared.
+// All eight softmax warps work on one query tile at a time, tile A then tile B for every key
+// tile. Warps w and w + 4 share TMEM lane quarter w % 4 (query rows 32 (w % 4) ... + 31); warp
+// w takes key columns 0..63 of the key tile and warp w + 4 columns 64..127. So the softmax of
+// one tile has two warps on every sub-partition while the MMAs of the other tile run, instead
+// of two tiles' softmaxes sharing the sub-partitions at once.
+struct TileState {
+  float m_run;       // running max of scaled scores (log2 units), kept key tiles only
+  float m_use;       // exponent reference of l and O (trails m_run by <= 8)
+  float l;           // this thread's half of the row sum, relative to m_use
+  int pv_count;      // kept key tiles so far
+  uint32_t skipped;  // skipped key tiles so far (counted by the leader thread)
+};
+
+__device__ __forceinline__ void swap_state(TileState& a, TileState& b) {
+  const TileState tmp = a;
+  a = b;
+  b = tmp;
+}
+
 template <bool kVarlen, bool kMaxProb>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
-                                            int b, int h, int t, int qt) {
+                                            int b, int h, int qt0) {
   const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
-  volatile uint32_t* quit = sm.quit[t];
-  const int wq = (threadIdx.x >> 5) & 3;  // warp inside the warpgroup == TMEM lane quarter
+  const int warp = threadIdx.x >> 5;
+  const int wq = warp & 3;                // TMEM lane quarter
+  const int half = warp >> 2;             // key columns 64 * half ... + 63; O features likewise
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;         // query row inside the tile == TMEM lane
-  const int q_row = qt * kTile + row;
-  const bool tile_exists = qt < g.nQ;
-  const bool row_valid = q_row < g.Sq;
-  const bool leader = row == 0;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + lane_base + col_s(t);
-  const uint32_t t_o = tmem + lane_base + col_o(t);
-  const uint32_t s_full = smem_u32(&sm.s_full[t]);
-  const uint32_t p_ready = smem_u32(&sm.p_ready[t]);
-  const uint32_t o_done = smem_u32(&sm.o_done[t]);
-  const size_t mask_base =
-      (p.skip_mask && tile_exists) ? ((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) : 0;
-
-  float m_run = -INFINITY;  // running max of scaled scores (log2 units), kept tiles only
-  float m_use = -INFINITY;  // exponent reference of l and O (trails m_run by <= 8)
-  float l = 0.f;
-  int pv_count = 0;
-  uint32_t skipped = 0;
+  const bool leader = threadIdx.x == 0;
+  TileState cur{-INFINITY, -INFINITY, 0.f, 0, 0u};  // the tile of the current step
+  TileState oth = cur;                              // the other tile
   bool failed = false;
   bool left_early = false;
 
-  for (int j = 0; j < L.nK(); ++j) {
+  for (int step = 0; step < 2 * L.nK(); ++step) {
+    const int t = step & 1;
+    const int j = step >> 1;
+    const int qt = qt0 + t;
+    const bool row_valid = qt * kTile + row < g.Sq;
+    const uint32_t t_s = tmem + lane_base + col_s(t);
     bool pass = true;
-    uint32_t sr[kTile];
-    float tm2 = 0.f;
+    float hmax = -INFINITY;
+    uint32_t sr[64];
     if (!failed) {
-      const bool ok = wait_bar(s_full, j & 1, abort, kErrSoftmax);
+      const bool ok = wait_bar(smem_u32(&sm.s_full[t]), j & 1, abort, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
     }
     if (!failed) {
       tc_fence_after();
-      tmem_ld128(t_s, sr);
-      const int valid_keys = L.Sk() - j * kTile;
-      if (valid_keys < kTile) {
+      tmem_ld64(t_s + half * 64, sr);
+      const int valid_keys = L.Sk() - j * kTile - half * 64;
+      if (valid_keys < 64) {
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= valid_keys) sr[c] = __float_as_uint(-INFINITY);
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTile; c += 8) {
+      for (int c = 0; c < 64; c += 8) {
         mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
         mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
         mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
         mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
       }
-      mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
-      tm2 = mx0 * p.scale_log2;
-      // The skip test for this row; rows past Sq do not exist and always pass.
-      pass = !row_valid || (tm2 - m_run < L.log2_lambda());
+      hmax = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+      sm.hmax[t][half][row] = hmax;
+      // A row passes when both of its halves pass; rows past Sq do not exist and always pass.
+      pass = !row_valid || (hmax * p.scale_log2 - cur.m_run < L.log2_lambda());
     } else {
-      quit[j & 1] = 1u;
+      sm.quit[t][j & 1] = 1u;
     }
-    const bool skip = bar_and<kSoftmaxThreads>(1u + static_cast<uint32_t>(t), pass);
-    if (quit[j & 1]) {  // written only before this barrier: the whole warpgroup sees one value
+    // The skip test over all 128 rows (both halves of each); the barrier also publishes hmax.
+    const bool skip = bar_and<2 * kSoftmaxThreads>(1u + static_cast<uint32_t>(t), pass);
+    if (*reinterpret_cast<volatile uint32_t*>(&sm.quit[t][j & 1])) {  // written only before this barrier
       left_early = true;
       break;
     }
-    if (leader) {
-      // Publish the decision: the producer loads V_j only if some tile keeps key tile j,
-      // and the MMA issues P V only for a kept tile.
-      sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
-      mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
-      if (tile_exists && p.skip_mask) p.skip_mask[mask_base + j] = skip ? 1 : 0;
-    }
-    if (skip) {
-      if (leader) ++skipped;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
-      continue;
-    }
+    do {
+      if (leader) {
+        // Publish the decision: the producer loads V_j only if some tile keeps key tile j,
+        // and the MMA issues P V only for a kept tile.
+        sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
+        mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
+        if (qt < g.nQ && p.skip_mask)
+          p.skip_mask[((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) + j] = skip ? 1 : 0;
+      }
+      if (skip) {
+        if (leader) ++cur.skipped;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready[t]));
+        break;
+      }
 
-    // Kept tile: online-softmax update.
-    const float m_new = fmaxf(m_run, tm2);
-    m_run = m_new;
-    float alpha = 1.f;
-    if (m_new - m_use > kRescaleThreshold) {
-      alpha = ex2_approx(m_use - m_new);  // 0 for the first kept tile
-      m_use = m_new;
-    }
-    // P = exp2(s * scale * log2 e - m_use), two columns per packed f32x2 FMA. P (bf16, keys
-    // 2c and 2c+1 in column c) overwrites the first 64 columns of S_j, written in two halves
-    // of 32 columns as it is produced.
-    const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
-    const uint64_t nref2 = pack_f32x2(-m_use, -m_use);
-    uint64_t sum_a = pack_f32x2(0.f, 0.f), sum_b = sum_a;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+      // Kept key tile: online-softmax update with the full row max.
+      const float tm2 = fmaxf(hmax, sm.hmax[t][half ^ 1][row]) * p.scale_log2;
+      const float m_new = fmaxf(cur.m_run, tm2);
+      cur.m_run = m_new;
+      float alpha = 1.f;
+      if (m_new - cur.m_use > kRescaleThreshold) {
+        alpha = ex2_approx(cur.m_use - m_new);  // 0 for the first kept tile
+        cur.m_use = m_new;
+      }
+      // P = exp2(s * scale * log2 e - m_use) for this thread's 64 keys, two per packed f32x2
+      // FMA; P (bf16, keys 2c and 2c + 1 in column c) overwrites columns 32 half ... + 31 of
+      // S_j. (Every thread read its scores before the vote barrier.)
+      const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
+      const uint64_t nref2 = pack_f32x2(-cur.m_use, -cur.m_use);
+      uint64_t sum_a = pack_f32x2(0.f, 0.f), sum_b = sum_a;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int k0 = half * 64 + 2 * c;
-        const uint64_t x2 = fma_f32x2(pack_f32x2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
-                                      scale2, nref2);
+        const uint64_t x2 =
+            fma_f32x2(pack_f32x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2, nref2);
         float x0, x1;
         unpack_f32x2(x2, x0, x1);
         const float p0 = ex2_approx(x0);
@@ -532,66 +544,86 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
         pk[c] = pack_bf16(p0, p1);
       }
       tmem_st32(t_s + half * 32, pk);
-    }
-    tmem_st_wait();
-    {
-      float a0, a1, b0, b1;
-      unpack_f32x2(sum_a, a0, a1);
-      unpack_f32x2(sum_b, b0, b1);
-      l = l * alpha + ((a0 + a1) + (b0 + b1));
-    }
-    // O is rescaled only by warps that need it. Every earlier P V of this tile has completed:
-    // S_j, which this thread waited for, was committed after them.
-    if (pv_count > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int c = 0; c < kHeadDim / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_o + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-        tmem_st32(t_o + c * 32, r);
-      }
       tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(p_ready);
-    ++pv_count;
+      {
+        float a0, a1, b0, b1;
+        unpack_f32x2(sum_a, a0, a1);
+        unpack_f32x2(sum_b, b0, b1);
+        cur.l = cur.l * alpha + ((a0 + a1) + (b0 + b1));
+      }
+      // O (this thread's 64 features) is rescaled only by warps that need it. Every earlier
+      // P V of this tile has completed: S_j, which this thread waited for, was committed
+      // after them.
+      if (cur.pv_count > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t t_o = tmem + lane_base + col_o(t) + half * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(t_o + c * 32, r);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready[t]));
+      ++cur.pv_count;
+    } while (false);
+    swap_state(cur, oth);
   }
+  if (left_early) return;
 
-  if (!left_early && !failed && pv_count > 0 && tile_exists) {
-    const bool ok = wait_bar(o_done, 0, abort, kErrSoftmax);
-    if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      __nv_bfloat16* orow =
-          p.o + ((out_tok0<kVarlen>(p, g, b) + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim;
+  // Epilogue: after 2 nK steps `cur` holds tile A and `oth` tile B. The two halves of each
+  // row combine their sums (same exponent reference), then write their 64 features of O.
+  sm.lpart[0][half][row] = cur.l;
+  sm.lpart[1][half][row] = oth.l;
+  bar_sync_n<2 * kSoftmaxThreads>(3u);
+  const bool ok = failed ? false : wait_bar(smem_u32(&sm.o_done[0]), 0, abort, kErrSoftmax) &&
+                                       wait_bar(smem_u32(&sm.o_done[1]), 0, abort, kErrSoftmax);
+  if (!__all_sync(0xffffffffu, ok)) return;
+  tc_fence_after();
+#pragma unroll 1
+  for (int t = 0; t < kQTiles; ++t) {
+    const TileState st = t ? oth : cur;
+    const int qt = qt0 + t;
+    const int q_row = qt * kTile + row;
+    const bool tile_exists = qt < g.nQ;
+    const bool row_valid = q_row < g.Sq;
+    if (leader && tile_exists && p.skip_counts && st.skipped)
+      atomicAdd(&p.skip_counts[static_cast<size_t>(b) * p.H + h], st.skipped);
+    if (!tile_exists || st.pv_count == 0) continue;
+    const float l = st.l + sm.lpart[t][half ^ 1][row];
+    const float inv_l = 1.f / l;
+    const uint32_t t_o = tmem + lane_base + col_o(t) + half * 64;
+    __nv_bfloat16* orow =
+        p.o + ((out_tok0<kVarlen>(p, g, b) + (row_valid ? q_row : 0)) * p.H + h) * kHeadDim + half * 64;
 #pragma unroll
-      for (int c = 0; c < kHeadDim / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_o + c * 32, r);
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+    for (int c = 0; c < 2; ++c) {
+      uint32_t r[32];
+      tmem_ld32(t_o + c * 32, r);
+      if (row_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-            w.y = pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-            w.z = pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-            w.w = pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-            dst[i] = w;
-          }
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+          w.y = pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+          w.z = pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+          w.w = pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+          dst[i] = w;
         }
       }
+    }
+    if (half == 0 && row_valid) {
       const size_t stat0 = stat_base<kVarlen>(p, g, b, h);
-      if (row_valid && p.lse) p.lse[stat0 + q_row] = (m_use + log2f(l)) * kLn2;
+      if (p.lse) p.lse[stat0 + q_row] = (st.m_use + log2f(l)) * kLn2;
       // The largest softmax weight of the row, exp(m - m) / l with l relative to the row
       // max m ("video-attention", "max_prob = 1 / l_i"): 2^(m_run - m_use) / l here.
-      if (kMaxProb && row_valid) p.max_prob[stat0 + q_row] = ex2_approx(m_run - m_use) * inv_l;
+      if (kMaxProb) p.max_prob[stat0 + q_row] = ex2_approx(st.m_run - st.m_use) * inv_l;
     }
   }
-  if (leader && tile_exists && p.skip_counts && skipped)
-    atomicAdd(&p.skip_counts[static_cast<size_t>(b) * p.H + h], skipped);
 }
 
 // One instance per feature set (packed documents, max_prob output), so that the plain
@@ -633,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.s_full[t]), 1);
       mbar_init(smem_u32(&sm.dec[t][0]), 1);
       mbar_init(smem_u32(&sm.dec[t][1]), 1);
-      mbar_init(smem_u32(&sm.p_ready[t]), kSoftmaxWarps);
+      mbar_init(smem_u32(&sm.p_ready[t]), kQTiles * kSoftmaxWarps);
       mbar_init(smem_u32(&sm.o_done[t]), 1);
       sm.skip_flag[t][0] = 0u;
       sm.skip_flag[t][1] = 0u;
@@ -666,8 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     regs_increase<kSoftmaxRegs>();
-    const int t = warp / kSoftmaxWarps;
-    run_softmax<kVarlen, kMaxProb>(sm, sm.tmem_base, p, g, b, h, t, qt0 + t);
+    run_softmax<kVarlen, kMaxProb>(sm, sm.tmem_base, p, g, b, h, qt0);
   }
 
   tc_fence_before();
