@@ -38,6 +38,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -118,6 +119,7 @@ struct FwdParams {
   const int* cu_k;
   int Tq, Tk;         // varlen: total query / key tokens (token extents of the packed tensors)
   int min_seq_len;    // documents with fewer keys than this run dense
+  int withhold_k;     // test of the bounded waits: the copy of this key tile is never issued (-1: off)
 };
 
 // What one CTA works on: one batch entry (or packed document) and head, and its lengths.
@@ -251,6 +253,10 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   int k_issued = 0, v_issued = 0;
   auto issue_k = [&](int j) {
     const int st = k_issued & 1;
+    if (j == p.withhold_k) {  // the waits on this copy run out (see launch())
+      ++k_issued;
+      return;
+    }
     const uint32_t kf = smem_u32(&sm.k_full[st]);
     const uint32_t ks = smem_u32(sm.k[st]);
     mbar_arrive_expect_tx(kf, kQKBytes);
@@ -870,6 +876,15 @@ blasst_status launch(const blasst_fwd_args& a) {
   p.Tq = a.Sq;
   p.Tk = a.Sk;
   p.min_seq_len = a.min_seq_len;
+  // Test switch for the bounded device waits: BLASST_TEST_WITHHOLD_K_TILE=j makes the producer
+  // skip the copy of key tile j, so the waits on it give up after their time limit, the CTA
+  // leaves through its abort path and blasst_device_error reports the role. Off when unset.
+  p.withhold_k = -1;
+  if (const char* w = std::getenv("BLASST_TEST_WITHHOLD_K_TILE")) {
+    char* end = nullptr;
+    const long v = std::strtol(w, &end, 10);
+    if (end != w && v >= 0 && v < 0x7fffffffL) p.withhold_k = static_cast<int>(v);
+  }
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
   if (a.skip_counts &&

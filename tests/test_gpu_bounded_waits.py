@@ -1,0 +1,55 @@
+"""GPU test of failure detection: a device-side wait that runs out gives up, the kernel
+leaves through its abort path, the host reads the error word, and the context stays usable.
+
+The failure is made by a test switch (environment variable BLASST_TEST_WITHHOLD_K_TILE)
+under which the producer never issues the copy of one key tile, so the waits on it run
+out after their time limit. Nothing faults: every device wait in the kernel is bounded."""
+import time
+
+import numpy as np
+import pytest
+
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+ERR_MMA = 1 << 1  # the MMA thread gave up waiting
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import softmax_threshold_tile_gb300 as blasst
+    blasst.build_library()
+    blasst.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("tile", [0, 1, 3])
+def test_withheld_key_tile_times_out_and_context_survives(monkeypatch, tile):
+    import torch
+    import softmax_threshold_tile_gb300 as blasst
+    q, k, v = parity.clustered_inputs(1, 2, 512, 512, seed=7)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    ref = blasst.attn_fwd(qd, kd, vd, 2.0, want_mask=True)
+    torch.cuda.synchronize()
+    assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
+
+    monkeypatch.setenv("BLASST_TEST_WITHHOLD_K_TILE", str(tile))
+    t0 = time.monotonic()
+    blasst.attn_fwd(qd, kd, vd, 2.0)           # enqueued: the failure shows on the device
+    st, word = blasst.blasst_device_error(clear=True)
+    elapsed = time.monotonic() - t0
+    monkeypatch.delenv("BLASST_TEST_WITHHOLD_K_TILE")
+    assert st == blasst.BLASST_ERR_TIMEOUT
+    assert word & ERR_MMA, f"error word {word:#x}"
+    assert elapsed < 20.0
+
+    again = blasst.attn_fwd(qd, kd, vd, 2.0, want_mask=True)
+    torch.cuda.synchronize()
+    assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
+    assert torch.equal(again.o, ref.o) and torch.equal(again.lse, ref.lse)
+    np.testing.assert_array_equal(again.skip_mask.cpu().numpy(), ref.skip_mask.cpu().numpy())
