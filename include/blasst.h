@@ -131,6 +131,50 @@ enum { BLASST_QK_BF16 = 0, BLASST_QK_E4M3 = 1 };
 
 blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
 
+/*
+ * Host-buffer call: blasst_attn_fwd on fixed-length tensors that live in HOST memory. The heads
+ * are streamed through a caller-provided device workspace in groups of heads_per_group: the
+ * host-to-device copies of one group overlap the kernel on the previous group and the
+ * device-to-host copies of the group before that. (The attention of a head does not depend on
+ * any other head, so the outputs equal those of blasst_attn_fwd bit for bit.)
+ *
+ *   q            HOST [B, Sq, H, 128] bf16.   k, v   HOST [B, Sk, H, 128] bf16.
+ *   o            HOST [B, Sq, H, 128] bf16 output.   lse   HOST [B, H, Sq] fp32 output or NULL.
+ *                Page-locked (pinned) host memory lets the copies overlap the kernels; pageable
+ *                memory works but serialises them.
+ *   workspace    DEVICE buffer, 256-byte aligned, of at least
+ *                blasst_host_workspace_bytes(B, H, Sq, Sk, heads_per_group) bytes, owned by the
+ *                caller; it must not be used by any other call until this one has completed.
+ *   heads_per_group  1 .. H (H need not be a multiple of it).
+ *   stream       the call starts after earlier work on `stream`, and work enqueued on `stream`
+ *                afterwards starts after the last copy back: the host outputs are complete and the
+ *                host inputs and the workspace free once `stream` reaches that point.
+ *
+ * The library owns two streams and seven events per device for this call, created at its first
+ * use on the device; calls on one device are enqueued one at a time (a library mutex). No
+ * device memory is allocated. Per-head skip counts and the skip mask are not available here.
+ * Same argument rules and return codes as blasst_attn_fwd; struct_size must be
+ * sizeof(blasst_host_args).
+ */
+typedef struct blasst_host_args {
+  uint32_t struct_size;
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  int B, H, Sq, Sk, d;
+  float scale, factor;
+  void *workspace;
+  size_t workspace_bytes;
+  int heads_per_group;
+  struct CUstream_st *stream;
+} blasst_host_args;
+
+/* Device workspace the host-buffer call needs (two groups of q, k, v, o and lse), or 0 when an
+ * argument is outside its domain. */
+size_t blasst_host_workspace_bytes(int B, int H, int Sq, int Sk, int heads_per_group);
+
+blasst_status blasst_attn_fwd_host(const blasst_host_args *args);
+
 /* A static, human-readable name for a status code. */
 const char *blasst_status_string(blasst_status s);
 

@@ -18,7 +18,12 @@ from ._binding import (  # noqa: F401
     AttnResult,
     BlasstError,
     FwdArgs,
+    HostArgs,
     attn_fwd,
+    attn_fwd_host,
+    host_workspace,
+    blasst_attn_fwd_host,
+    blasst_host_workspace_bytes,
     attn_varlen_fwd,
     blasst_attn_fwd_ex,
     blasst_attn_fwd,

@@ -46,6 +46,20 @@ class FwdArgs(ctypes.Structure):
     ]
 
 
+class HostArgs(ctypes.Structure):
+    """Mirror of ``blasst_host_args`` (include/blasst.h)."""
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("Sq", ctypes.c_int), ("Sk", ctypes.c_int), ("d", ctypes.c_int),
+        ("scale", ctypes.c_float), ("factor", ctypes.c_float),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("heads_per_group", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 class BlasstError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {blasst_status_string(code)} (status {code})")
@@ -73,6 +87,10 @@ def load_library(path: str | None = None):
                                     ctypes.c_float, ctypes.c_float, vp, vp, u8p]
     lib.blasst_attn_fwd_ex.restype = ctypes.c_int
     lib.blasst_attn_fwd_ex.argtypes = [ctypes.POINTER(FwdArgs)]
+    lib.blasst_attn_fwd_host.restype = ctypes.c_int
+    lib.blasst_attn_fwd_host.argtypes = [ctypes.POINTER(HostArgs)]
+    lib.blasst_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.blasst_host_workspace_bytes.argtypes = [ctypes.c_int] * 5
     lib.blasst_status_string.restype = ctypes.c_char_p
     lib.blasst_status_string.argtypes = [ctypes.c_int]
     lib.blasst_device_error.restype = ctypes.c_int
@@ -127,6 +145,25 @@ def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor
     a.max_seqlen_q, a.max_seqlen_k, a.min_seq_len = int(max_seqlen_q), int(max_seqlen_k), int(min_seq_len)
     a.qk_format, a.q_descale, a.k_descale = int(qk_format), float(q_descale), float(k_descale)
     return int(load_library().blasst_attn_fwd_ex(ctypes.byref(a)))
+
+
+def blasst_host_workspace_bytes(B, H, Sq, Sk, heads_per_group) -> int:
+    return int(load_library().blasst_host_workspace_bytes(int(B), int(H), int(Sq), int(Sk), int(heads_per_group)))
+
+
+def blasst_attn_fwd_host(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, workspace, workspace_bytes,
+                         heads_per_group, stream) -> int:
+    """The host-buffer C entry point: q / k / v / o / lse are HOST addresses (or CPU tensors),
+    workspace a device address (or CUDA tensor)."""
+    a = HostArgs()
+    a.struct_size = ctypes.sizeof(HostArgs)
+    a.q, a.k, a.v, a.o, a.lse = _p(q), _p(k), _p(v), _p(o), _p(lse)
+    a.B, a.H, a.Sq, a.Sk, a.d = int(B), int(H), int(Sq), int(Sk), int(d)
+    a.scale, a.factor = float(scale), float(factor)
+    a.workspace, a.workspace_bytes = _p(workspace), int(workspace_bytes)
+    a.heads_per_group = int(heads_per_group)
+    a.stream = _p(stream)
+    return int(load_library().blasst_attn_fwd_host(ctypes.byref(a)))
 
 
 def blasst_status_string(code: int) -> str:
@@ -247,3 +284,41 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
     if st != BLASST_OK:
         raise BlasstError(st, "blasst_attn_fwd_ex")
     return AttnResult(o, lse, counts, None, mp)
+
+
+def host_workspace(B: int, H: int, Sq: int, Sk: int, heads_per_group: int, device=None):
+    """A device workspace (uint8 CUDA tensor) large enough for attn_fwd_host."""
+    import torch
+    n = blasst_host_workspace_bytes(B, H, Sq, Sk, heads_per_group)
+    if n == 0:
+        raise ValueError("invalid sizes for the host-buffer call")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def attn_fwd_host(q, k, v, factor: float, scale: float | None = None, *, out=None, lse=None, workspace=None,
+                  heads_per_group: int | None = None, stream=None):
+    """Skip-Softmax attention on HOST tensors [B, S, H, 128] bf16 (contiguous CPU tensors; pinned for
+    overlap), streamed through a device workspace by head groups. Returns (o, lse) CPU tensors; they
+    are complete once `stream` (default: the current stream) has reached the end of the call."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous() or t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CPU bf16 tensor [B, S, H, 128]")
+    B, Sq, H, d = q.shape
+    Sk = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if heads_per_group is None:
+        heads_per_group = max(1, (H + 3) // 4)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned())
+    if workspace is None:
+        workspace = host_workspace(B, H, Sq, Sk, heads_per_group)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    st = blasst_attn_fwd_host(q, k, v, out, lse, B, H, Sq, Sk, d, scale, factor, workspace,
+                              workspace.numel() * workspace.element_size(), heads_per_group, stream.cuda_stream)
+    if st != BLASST_OK:
+        raise BlasstError(st, "blasst_attn_fwd_host")
+    return out, lse

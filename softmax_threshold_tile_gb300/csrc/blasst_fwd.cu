@@ -907,6 +907,162 @@ blasst_status launch(const blasst_fwd_args& a) {
 }  // namespace
 }  // namespace blasst
 
+namespace blasst {
+namespace {
+
+// ------------------------------------------------------------------ host-buffer streaming
+constexpr size_t kWsAlign = 256;
+size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+// One workspace slot holds a head group's q, k, v, o and lse.
+struct HostSlot {
+  size_t q, k, v, o, lse, bytes;  // byte offsets inside the slot, and its size
+};
+HostSlot host_slot(int B, int Sq, int Sk, int hg) {
+  HostSlot s{};
+  const size_t row = static_cast<size_t>(hg) * kHeadDim * 2;
+  s.q = 0;
+  s.o = s.q + round_up(static_cast<size_t>(B) * Sq * row);
+  s.k = s.o + round_up(static_cast<size_t>(B) * Sq * row);
+  s.v = s.k + round_up(static_cast<size_t>(B) * Sk * row);
+  s.lse = s.v + round_up(static_cast<size_t>(B) * Sk * row);
+  s.bytes = s.lse + round_up(static_cast<size_t>(B) * hg * Sq * sizeof(float));
+  return s;
+}
+
+bool host_dims_ok(int B, int H, int Sq, int Sk, int hg) {
+  return B > 0 && H > 0 && Sq > 0 && Sk > 0 && B <= 65535 && H <= 65535 && hg >= 1 && hg <= H;
+}
+
+// Streams and events of the host-buffer call, one set per device, made at its first use there.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex;
+
+bool make_pipe(HostPipe& hp) {
+  if (hp.ready) return true;
+  bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < 2 && ok; ++i)
+    ok = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.comp_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return false;
+  }
+  hp.ready = true;
+  return true;
+}
+
+blasst_status launch_host(const blasst_host_args& a) {
+  // ---- argument checks: no CUDA call happens before all of them pass
+  if (!a.q || !a.k || !a.v || !a.o || !a.workspace) return BLASST_ERR_INVALID_ARG;
+  if (!host_dims_ok(a.B, a.H, a.Sq, a.Sk, a.heads_per_group) || a.d != kHeadDim) return BLASST_ERR_INVALID_ARG;
+  if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return BLASST_ERR_INVALID_ARG;
+  if (!std::isfinite(a.factor) || !(a.factor >= 0.f)) return BLASST_ERR_INVALID_ARG;
+  if (!aligned(a.workspace, kWsAlign)) return BLASST_ERR_INVALID_ARG;
+  const int hg = a.heads_per_group;
+  const HostSlot slot = host_slot(a.B, a.Sq, a.Sk, hg);
+  if (a.workspace_bytes < 2 * slot.bytes) return BLASST_ERR_INVALID_ARG;
+  const double batch_stride = 256.0 * a.H * static_cast<double>(a.Sq > a.Sk ? a.Sq : a.Sk);
+  if (batch_stride >= 1099511627776.0) return BLASST_ERR_INVALID_ARG;
+
+  const blasst_status ds = prepare_device();
+  if (ds != BLASST_OK) return ds;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BLASST_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  HostPipe& hp = g_pipe[dev];
+  if (!make_pipe(hp)) return BLASST_ERR_LAUNCH;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(a.stream);
+  const size_t hrow = static_cast<size_t>(a.H) * kHeadDim * 2;  // host bytes per (batch, token)
+  bool ok = cudaEventRecord(hp.start, cs) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
+  const int groups = (a.H + hg - 1) / hg;
+  blasst_status kst = BLASST_OK;
+  for (int g = 0; g < groups && ok; ++g) {
+    const int s = g & 1;
+    const int h0 = g * hg;
+    const int hc = a.H - h0 < hg ? a.H - h0 : hg;
+    const size_t crow = static_cast<size_t>(hc) * kHeadDim * 2;  // device bytes per (batch, token)
+    uint8_t* base = static_cast<uint8_t*>(a.workspace) + s * slot.bytes;
+    const size_t hoff = static_cast<size_t>(h0) * kHeadDim * 2;
+    // The kernel of group g - 2 read this slot's q, k, v; the copy-out of group g - 2 read its o, lse.
+    if (g >= 2) ok = cudaStreamWaitEvent(hp.in, hp.comp_done[s], 0) == cudaSuccess;
+    ok = ok &&
+         cudaMemcpy2DAsync(base + slot.q, crow, static_cast<const uint8_t*>(a.q) + hoff, hrow, crow,
+                           static_cast<size_t>(a.B) * a.Sq, cudaMemcpyHostToDevice, hp.in) == cudaSuccess &&
+         cudaMemcpy2DAsync(base + slot.k, crow, static_cast<const uint8_t*>(a.k) + hoff, hrow, crow,
+                           static_cast<size_t>(a.B) * a.Sk, cudaMemcpyHostToDevice, hp.in) == cudaSuccess &&
+         cudaMemcpy2DAsync(base + slot.v, crow, static_cast<const uint8_t*>(a.v) + hoff, hrow, crow,
+                           static_cast<size_t>(a.B) * a.Sk, cudaMemcpyHostToDevice, hp.in) == cudaSuccess &&
+         cudaEventRecord(hp.in_done[s], hp.in) == cudaSuccess &&
+         cudaStreamWaitEvent(cs, hp.in_done[s], 0) == cudaSuccess;
+    if (ok && g >= 2) ok = cudaStreamWaitEvent(cs, hp.out_done[s], 0) == cudaSuccess;
+    if (!ok) break;
+    blasst_fwd_args fa{};
+    fa.struct_size = sizeof(fa);
+    fa.q = base + slot.q;
+    fa.k = base + slot.k;
+    fa.v = base + slot.v;
+    fa.o = base + slot.o;
+    fa.lse = a.lse ? reinterpret_cast<float*>(base + slot.lse) : nullptr;
+    fa.B = a.B;
+    fa.H = hc;
+    fa.Sq = a.Sq;
+    fa.Sk = a.Sk;
+    fa.d = a.d;
+    fa.scale = a.scale;
+    fa.factor = a.factor;
+    fa.stream = a.stream;
+    kst = launch(fa);
+    if (kst != BLASST_OK) break;
+    ok = cudaEventRecord(hp.comp_done[s], cs) == cudaSuccess &&
+         cudaStreamWaitEvent(hp.out, hp.comp_done[s], 0) == cudaSuccess &&
+         cudaMemcpy2DAsync(static_cast<uint8_t*>(a.o) + hoff, hrow, base + slot.o, crow, crow,
+                           static_cast<size_t>(a.B) * a.Sq, cudaMemcpyDeviceToHost, hp.out) == cudaSuccess;
+    if (ok && a.lse)  // device [B, hc, Sq] -> host rows (b H + h0) Sq ... of [B, H, Sq]
+      ok = cudaMemcpy2DAsync(a.lse + static_cast<size_t>(h0) * a.Sq, static_cast<size_t>(a.H) * a.Sq * sizeof(float),
+                             base + slot.lse, static_cast<size_t>(hc) * a.Sq * sizeof(float),
+                             static_cast<size_t>(hc) * a.Sq * sizeof(float), a.B, cudaMemcpyDeviceToHost,
+                             hp.out) == cudaSuccess;
+    ok = ok && cudaEventRecord(hp.out_done[s], hp.out) == cudaSuccess;
+  }
+  // Later work on the caller's stream starts after the last copy back.
+  const bool tail = cudaEventRecord(hp.out_done[0], hp.out) == cudaSuccess &&
+                    cudaStreamWaitEvent(cs, hp.out_done[0], 0) == cudaSuccess;
+  if (kst != BLASST_OK) return kst;
+  if (!ok || !tail) {
+    cudaGetLastError();
+    return BLASST_ERR_LAUNCH;
+  }
+  return BLASST_OK;
+}
+
+}  // namespace
+}  // namespace blasst
+
+extern "C" size_t blasst_host_workspace_bytes(int B, int H, int Sq, int Sk, int heads_per_group) {
+  if (!blasst::host_dims_ok(B, H, Sq, Sk, heads_per_group)) return 0;
+  return 2 * blasst::host_slot(B, Sq, Sk, heads_per_group).bytes;
+}
+
+extern "C" blasst_status blasst_attn_fwd_host(const blasst_host_args* args) {
+  if (!args || args->struct_size != sizeof(blasst_host_args)) return BLASST_ERR_INVALID_ARG;
+  return blasst::launch_host(*args);
+}
+
 extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const void* v, void* o,
                                          float* lse, int B, int H, int Sq, int Sk, int d,
                                          float scale, float factor, struct CUstream_st* stream,
@@ -969,4 +1125,4 @@ extern "C" blasst_status blasst_device_error(uint32_t* word, int clear) {
   return w ? BLASST_ERR_TIMEOUT : BLASST_OK;
 }
 
-extern "C" int blasst_version(void) { return 10100; }
+extern "C" int blasst_version(void) { return 10200; }

@@ -136,3 +136,51 @@ def test_extended_rejects_wrong_struct_size(lib):
     a.struct_size = ctypes.sizeof(blasst.FwdArgs) - 4
     assert lib.blasst_attn_fwd_ex(ctypes.byref(a)) == blasst.BLASST_ERR_INVALID_ARG
     assert lib.blasst_attn_fwd_ex(None) == blasst.BLASST_ERR_INVALID_ARG
+
+
+def test_host_args_struct_matches_header(tmp_path):
+    import ctypes
+    src = tmp_path / "hsize.c"
+    src.write_text('#include <stdio.h>\n#include "blasst.h"\nint main(void){printf("%zu\\n", sizeof(blasst_host_args));return 0;}\n')
+    exe = tmp_path / "hsize"
+    subprocess.check_call(["gcc", "-I", INCLUDE, str(src), "-o", str(exe)])
+    size = int(subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout)
+    assert size == ctypes.sizeof(blasst.HostArgs)
+
+
+def test_host_workspace_bytes(lib):
+    B, H, Sq, Sk, hg = 2, 5, 1000, 777, 2
+    n = blasst.blasst_host_workspace_bytes(B, H, Sq, Sk, hg)
+    # two slots, each holding q, o (B Sq hg 256 B), k, v (B Sk hg 256 B) and lse (B hg Sq 4 B), 256-B aligned
+    per = 2 * B * Sq * hg * 256 + 2 * B * Sk * hg * 256 + B * hg * Sq * 4
+    assert 2 * per <= n <= 2 * (per + 5 * 256) and n % 256 == 0
+    assert blasst.blasst_host_workspace_bytes(B, H, Sq, Sk, H) > n
+    for bad in ((0, H, Sq, Sk, hg), (B, H, Sq, Sk, 0), (B, H, Sq, Sk, H + 1), (B, H, 0, Sk, hg)):
+        assert blasst.blasst_host_workspace_bytes(*bad) == 0
+
+
+def call_host(**kw):
+    B, H, Sq, Sk = 2, 3, 500, 400
+    a = dict(q=4096, k=8192, v=12288, o=16384, lse=None, B=B, H=H, Sq=Sq, Sk=Sk, d=128,
+             scale=1 / math.sqrt(128), factor=2.0, workspace=1 << 20,
+             workspace_bytes=blasst.blasst_host_workspace_bytes(B, H, Sq, Sk, 2), heads_per_group=2, stream=None)
+    a.update(kw)
+    return blasst.blasst_attn_fwd_host(**a)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(o=0), dict(workspace=0), dict(d=64), dict(B=0), dict(Sk=0),
+    dict(heads_per_group=0), dict(heads_per_group=4),
+    dict(workspace=(1 << 20) + 16),                      # not 256-byte aligned
+    dict(workspace_bytes=1000),                          # too small
+    dict(scale=0.0), dict(factor=-1.0), dict(factor=float("nan")),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_host_call_invalid_arguments(lib, kw):
+    assert call_host(**kw) == blasst.BLASST_ERR_INVALID_ARG
+
+
+def test_host_call_rejects_wrong_struct_size(lib):
+    import ctypes
+    a = blasst.HostArgs()
+    a.struct_size = ctypes.sizeof(blasst.HostArgs) + 8
+    assert lib.blasst_attn_fwd_host(ctypes.byref(a)) == blasst.BLASST_ERR_INVALID_ARG
