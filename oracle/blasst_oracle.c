@@ -20,8 +20,7 @@
  *   "Skip-Softmax" (docs.vllm.ai), section "The online-softmax pass":
  *       key tiles of 128; tile scores are Q . K_j^T . scale.
  *
- * Readings where the pages are silent (each is listed with its reason in the
- * design notes of the repository):
+ * Readings where the cited sections are silent:
  *   - query tiles are 128 rows by default (tile_q is a parameter for small tests);
  *   - running_max is the row maximum over the tiles already accumulated, taken
  *     before tile j; a skipped tile leaves m, l and O unchanged;

@@ -27,7 +27,7 @@
 //
 // Numerics: scores are fp32 from bf16 operands; the test is evaluated in log2
 // units, (tile_max - running_max) * scale * log2(e) < log2(lambda), which is the
-// pages' log-space test scaled by log2(e). P is rounded to bf16 for P V; l and O
+// design doc's log-space test scaled by log2(e). P is rounded to bf16 for P V; l and O
 // accumulate in fp32. The exponent reference m_use trails the true running max
 // by at most 8 (log2 units), so O is rescaled only when the max grows by more
 // than that; the skip test always uses the true running max.

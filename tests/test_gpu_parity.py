@@ -70,7 +70,7 @@ def test_odd_shapes(Sq, Sk, factor):
 
 
 def test_large_factor_lambda_above_one():
-    """lambda > 1 is allowed and computed literally (the decision is still the pages' test)."""
+    """lambda > 1 is allowed and computed literally (the decision is still the design doc's test)."""
     q, k, v = parity.clustered_inputs(1, 2, 512, 512, seed=11)
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
     f = 2048.0  # lambda = 4

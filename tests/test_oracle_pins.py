@@ -1,4 +1,4 @@
-"""Pins for the CPU oracle, against facts fixed by the pages and by mathematics.
+"""Pins for the CPU oracle, against facts fixed by the cited sources and by mathematics.
 
 Each check below would fail on a plausible mistake in ``oracle/blasst_oracle.c``
 (``test_oracle_mutants.py`` plants such mistakes and confirms it):
