@@ -329,9 +329,16 @@ def run_ours(args, w):
             ms = time_calls(blasst, stream, lambda: call(f), n_sweep)
             skip = float(m.mean())
             ex = executed_flops(w, m)
-            sweep.append({"factor": f, "lambda": f / S, "skip_fraction": skip, "ms": ms,
-                          "exec_tflops": ex / ms / 1e9, "dense_equiv_tflops": dense / ms / 1e9,
-                          "tensor_frac": ex / ms / 1e9 / peak_burst})
+            entry = {"factor": f, "lambda": f / S, "skip_fraction": skip, "ms": ms,
+                     "exec_tflops": ex / ms / 1e9, "dense_equiv_tflops": dense / ms / 1e9,
+                     "tensor_frac": ex / ms / 1e9 / peak_burst}
+            if B > 1:
+                entry["skip_fraction_per_batch"] = [round(float(x), 4) for x in m.reshape(B, -1).mean(1)]
+            if w.gamma_range is not None:  # per-head structure: report the spread over heads
+                per_head = m.reshape(B, H, -1).mean(2).ravel()
+                entry["skip_fraction_per_head"] = {"min": float(per_head.min()), "median": float(np.median(per_head)),
+                                                   "max": float(per_head.max())}
+            sweep.append(entry)
         base = next((s["ms"] for s in sweep if s["factor"] == 0.0), None)
         for s in sweep:
             s["speedup_vs_dense"] = base / s["ms"] if base else None
