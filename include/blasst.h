@@ -145,7 +145,9 @@ blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
  *   workspace    DEVICE buffer, 256-byte aligned, of at least
  *                blasst_host_workspace_bytes(B, H, Sq, Sk, heads_per_group) bytes, owned by the
  *                caller; it must not be used by any other call until this one has completed.
- *   heads_per_group  1 .. H (H need not be a multiple of it).
+ *   heads_per_group  1 .. H (H need not be a multiple of it): the largest group. Group sizes
+ *                grow 1, 2, 4, ... up to it and the last group holds a single head, which
+ *                shortens the pipeline's fill and drain.
  *   stream       the call starts after earlier work on `stream`, and work enqueued on `stream`
  *                afterwards starts after the last copy back: the host outputs are complete and the
  *                host inputs and the workspace free once `stream` reaches that point.

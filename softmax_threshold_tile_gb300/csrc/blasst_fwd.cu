@@ -989,12 +989,15 @@ blasst_status launch_host(const blasst_host_args& a) {
   bool ok = cudaEventRecord(hp.start, cs) == cudaSuccess &&
             cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
-  const int groups = (a.H + hg - 1) / hg;
+  // Groups of heads: sizes 1, 2, 4, ... up to hg, so that each group's copy-in is about as long
+  // as the previous group's kernel (a short pipeline fill), and a single head last (a short
+  // drain).
   blasst_status kst = BLASST_OK;
-  for (int g = 0; g < groups && ok; ++g) {
+  int want = 1;
+  for (int g = 0, h0 = 0, hc = 0; h0 < a.H && ok; ++g, h0 += hc, want = want * 2 < hg ? want * 2 : hg) {
+    const int rem = a.H - h0;
+    hc = rem > want ? want : (rem > 1 && g > 0 ? rem - 1 : rem);
     const int s = g & 1;
-    const int h0 = g * hg;
-    const int hc = a.H - h0 < hg ? a.H - h0 : hg;
     const size_t crow = static_cast<size_t>(hc) * kHeadDim * 2;  // device bytes per (batch, token)
     uint8_t* base = static_cast<uint8_t*>(a.workspace) + s * slot.bytes;
     const size_t hoff = static_cast<size_t>(h0) * kHeadDim * 2;
