@@ -10,11 +10,13 @@
 //
 // One CTA owns two 128-row query tiles (A and B) of one (batch, head) and streams
 // every key tile once for both through a warp-specialised pipeline:
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one query row per
-//              thread (= TMEM lane). tcgen05.ld of S_j, row max, an AND-vote of
-//              the skip test over the tile's 128 rows (named barrier), exp2 of a
-//              kept tile written back into TMEM as bf16 P (over S_j), conditional
-//              O rescale, epilogue (O / l -> bf16, lse).
+//   warps 0-7  softmax, all eight on one tile at a time (A, then B, for every key
+//              tile): warps w and w + 4 share the TMEM lanes of rows 32 (w % 4) ...
+//              + 31 and take key columns 0-63 and 64-127. tcgen05.ld of S_j, half-row
+//              max, an AND-vote of the skip test over the tile's 128 rows (named
+//              barrier, which also publishes the half-row maxima), exp2 of a kept
+//              tile written back into TMEM as bf16 P (over S_j), conditional O
+//              rescale, epilogue (O / l -> bf16, lse).
 //   warp 8     MMA: one thread issues tcgen05.mma, alternating the two tiles so
 //              that one tile's softmax overlaps the other tile's matrix work:
 //                O_A += P_A(j) V_j ; S_A = Q_A K_{j+1}^T ; O_B += P_B(j) V_j ; S_B = Q_B K_{j+1}^T
