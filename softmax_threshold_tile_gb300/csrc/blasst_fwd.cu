@@ -225,7 +225,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ producer
-template <bool kVarlen, bool kFp8>
+template <bool kVarlen, bool kFp8, bool kDense>
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
                                              const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
                                              int qt0) {
@@ -277,7 +277,18 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   };
   issue_k(0);
   bool ok = true;
-  for (int j = 0; j < L.nK() && ok; ++j) {
+  if (kDense) {
+    // lambda = 0: every key tile is kept, so no decision is waited for. K_(j+1) and V_j go out
+    // together, and the stages are released by the scores instead: S_B(j) is committed after
+    // every MMA up to Q_B K_j^T, which covers the readers of K_j and of V_(j-1), the tiles the
+    // next iteration's copies overwrite.
+    for (int j = 0; j < L.nK() && ok; ++j) {
+      if (j + 1 < L.nK()) issue_k(j + 1);
+      issue_v(j);
+      ok = wait_bar(smem_u32(&sm.s_full[kQTiles - 1]), j & 1, abort, kErrProducer);
+    }
+  }
+  for (int j = 0; j < L.nK() && ok && !kDense; ++j) {
     if (j + 1 < L.nK()) issue_k(j + 1);
     // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
     // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
@@ -306,7 +317,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <bool kVarlen, bool kFp8>
+template <bool kVarlen, bool kFp8, bool kDense>
 __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
   const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
@@ -387,7 +398,8 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
         // key tile, after P is written (and O rescaled) for a kept one.
         if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
+        // (lambda = 0 keeps every key tile: no decision to read.)
+        const uint32_t skip = kDense ? 0u : *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
         if (!skip) {
           if (!v_ready) {
             if (!wait_bar(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
@@ -444,7 +456,7 @@ __device__ __forceinline__ void swap_state(TileState& a, TileState& b) {
   b = tmp;
 }
 
-template <bool kVarlen, bool kMaxProb>
+template <bool kVarlen, bool kMaxProb, bool kDense>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
                                             int b, int h, int qt0) {
   const Lens<kVarlen> L{p, g};
@@ -507,9 +519,12 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     do {
       if (leader) {
         // Publish the decision: the producer loads V_j only if some tile keeps key tile j,
-        // and the MMA issues P V only for a kept tile.
-        sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
-        mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
+        // and the MMA issues P V only for a kept tile. (With lambda = 0 both act on every
+        // key tile without it.)
+        if (!kDense) {
+          sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
+          mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
+        }
         if (qt < g.nQ && p.skip_mask)
           p.skip_mask[((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) + j] = skip ? 1 : 0;
       }
@@ -634,9 +649,9 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   }
 }
 
-// One instance per feature set (packed documents, max_prob output), so that the plain
-// fixed-length instance keeps the code generation of a kernel without them.
-template <bool kVarlen, bool kMaxProb, bool kFp8>
+// One instance per feature set (packed documents, max_prob output, e4m3 scores, lambda = 0),
+// so that the plain fixed-length instance keeps the code generation of a kernel without them.
+template <bool kVarlen, bool kMaxProb, bool kFp8, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
     blasst_fwd_sm103a(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k,
@@ -698,15 +713,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer<kVarlen, kFp8>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
+      if (lane == 0) run_producer<kVarlen, kFp8, kDense>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma<kVarlen, kFp8>(sm, sm.tmem_base, p, g);
+      if (lane == 0) run_mma<kVarlen, kFp8, kDense>(sm, sm.tmem_base, p, g);
       __syncwarp();
     }
   } else {
     regs_increase<kSoftmaxRegs>();
-    run_softmax<kVarlen, kMaxProb>(sm, sm.tmem_base, p, g, b, h, qt0);
+    run_softmax<kVarlen, kMaxProb, kDense>(sm, sm.tmem_base, p, g, b, h, qt0);
   }
 
   tc_fence_before();
@@ -757,17 +772,32 @@ bool encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, bool e
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K).
+// The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K,
+// 8 = lambda = 0).
+template <int kBits>
+const void* instance() {
+  return reinterpret_cast<const void*>(
+      blasst_fwd_sm103a<(kBits & 1) != 0, (kBits & 2) != 0, (kBits & 4) != 0, (kBits & 8) != 0>);
+}
+constexpr int kInstances = 16;
 const void* kernel_for(int bits) {
-  switch (bits & 7) {
-    case 0: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false, false>);
-    case 1: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false, false>);
-    case 2: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true, false>);
-    case 3: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true, false>);
-    case 4: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, false, true>);
-    case 5: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, false, true>);
-    case 6: return reinterpret_cast<const void*>(blasst_fwd_sm103a<false, true, true>);
-    default: return reinterpret_cast<const void*>(blasst_fwd_sm103a<true, true, true>);
+  switch (bits & (kInstances - 1)) {
+    case 0: return instance<0>();
+    case 1: return instance<1>();
+    case 2: return instance<2>();
+    case 3: return instance<3>();
+    case 4: return instance<4>();
+    case 5: return instance<5>();
+    case 6: return instance<6>();
+    case 7: return instance<7>();
+    case 8: return instance<8>();
+    case 9: return instance<9>();
+    case 10: return instance<10>();
+    case 11: return instance<11>();
+    case 12: return instance<12>();
+    case 13: return instance<13>();
+    case 14: return instance<14>();
+    default: return instance<15>();
   }
 }
 
@@ -796,7 +826,7 @@ blasst_status prepare_device() {
     return BLASST_ERR_UNSUPPORTED_DEVICE;
   }
   bool attr_ok = true;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < kInstances; ++i)
     attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(i), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(kSmemBytes)) == cudaSuccess;
   if (!attr_ok) {
@@ -895,7 +925,10 @@ blasst_status launch(const blasst_fwd_args& a) {
     return BLASST_ERR_LAUNCH;
   }
   void* args[] = {&tq, &tk, &tv, &p};
-  const void* kernel = kernel_for((varlen ? 1 : 0) | (a.max_prob ? 2 : 0) | (e4m3 ? 4 : 0));
+  // lambda = 0 (factor 0, or one length below min_seq_len) can skip nothing: the instance
+  // for it neither publishes nor waits for decisions.
+  const bool dense = !(p.log2_lambda > -INFINITY);
+  const void* kernel = kernel_for((varlen ? 1 : 0) | (a.max_prob ? 2 : 0) | (e4m3 ? 4 : 0) | (dense ? 8 : 0));
   const cudaError_t e = cudaLaunchKernel(kernel,
                                          dim3((p.nQ + kQTiles - 1) / kQTiles, a.H, a.B), dim3(kThreads), args,
                                          kSmemBytes, st);
