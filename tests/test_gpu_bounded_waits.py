@@ -31,19 +31,20 @@ def _gpu():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("factor", [2.0, 0.0])   # the general instance and the lambda = 0 one
 @pytest.mark.parametrize("tile", [0, 1, 3])
-def test_withheld_key_tile_times_out_and_context_survives(monkeypatch, tile):
+def test_withheld_key_tile_times_out_and_context_survives(monkeypatch, tile, factor):
     import torch
     import softmax_threshold_tile_gb300 as blasst
     q, k, v = parity.clustered_inputs(1, 2, 512, 512, seed=7)
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
-    ref = blasst.attn_fwd(qd, kd, vd, 2.0, want_mask=True)
+    ref = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True)
     torch.cuda.synchronize()
     assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
 
     monkeypatch.setenv("BLASST_TEST_WITHHOLD_K_TILE", str(tile))
     t0 = time.monotonic()
-    blasst.attn_fwd(qd, kd, vd, 2.0)           # enqueued: the failure shows on the device
+    blasst.attn_fwd(qd, kd, vd, factor)        # enqueued: the failure shows on the device
     st, word = blasst.blasst_device_error(clear=True)
     elapsed = time.monotonic() - t0
     monkeypatch.delenv("BLASST_TEST_WITHHOLD_K_TILE")
@@ -52,7 +53,7 @@ def test_withheld_key_tile_times_out_and_context_survives(monkeypatch, tile):
     assert (word & ~0x1f) == 0, f"error word {word:#x}"
     assert elapsed < 20.0
 
-    again = blasst.attn_fwd(qd, kd, vd, 2.0, want_mask=True)
+    again = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True)
     torch.cuda.synchronize()
     assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
     assert torch.equal(again.o, ref.o) and torch.equal(again.lse, ref.lse)
