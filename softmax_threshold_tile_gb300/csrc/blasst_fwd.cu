@@ -24,6 +24,8 @@
 //   warp 9     TMA producer: both Q tiles once, K tiles one ahead through a 2-stage ring,
 //              and V_j only once a tile has kept key tile j (as soon as tile A keeps it,
 //              otherwise after tile B's decision): a key tile both tiles skip is never loaded.
+// With lambda = 0 (and bf16 scores) nothing can be skipped: a separate instance publishes
+// and reads no decisions, and copies every V_j together with K_(j+1).
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Shared memory: Q_A, Q_B, 2 x K, 2 x V tiles of 32 KiB, all 128-byte swizzled.
 //
@@ -55,8 +57,8 @@ using namespace ptx;
 constexpr int kTile = 128;      // query rows per query tile == keys per key tile
 constexpr int kHeadDim = 128;   // d
 constexpr int kQTiles = 2;      // query tiles per CTA
-constexpr int kSoftmaxWarps = 4;             // per query tile
-constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kSoftmaxWarps = 4;             // warps that cover the 128 TMEM lanes once
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;  // the softmax runs kQTiles x this many threads
 constexpr int kMmaWarp = kQTiles * kSoftmaxWarps;   // 8
 constexpr int kLoadWarp = kMmaWarp + 1;             // 9
 constexpr int kThreads = 3 * 128;                   // 384: two softmax warpgroups + one for MMA / TMA
@@ -110,7 +112,7 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base
 
 struct FwdParams {
   int B, H, Sq, Sk, nQ, nK;  // fixed-length batch; in varlen mode Sq / Sk are the maxima
-  float scale_log2;   // scale * log2(e)
+  float scale_log2;   // scale (times both descales for e4m3 Q / K) * log2(e)
   float log2_lambda;  // log2(factor / Sk); -inf when factor == 0
   __nv_bfloat16* o;
   float* lse;
