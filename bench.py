@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads-per-group", type=int, default=0,
-                    help="largest head group of the end-to-end host-buffer call (0: 2 H / 5)")
+                    help="largest head group of the end-to-end host-buffer call (0: H / 5)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the max_prob, packed-document and FP8 timings")
     ap.add_argument("--cpu-units", type=int, default=48, help="query tiles in the CPU oracle sample")
@@ -449,7 +449,7 @@ def run_ours(args, w):
         qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q, k, v))
         oh = torch.empty(od.shape, dtype=torch.bfloat16).pin_memory()
         lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        hpg = args.heads_per_group or max(1, (2 * H) // 5)
+        hpg = args.heads_per_group or max(1, H // 5)
         ws_bytes = blasst.blasst_host_workspace_bytes(B, H, S, S, hpg)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         n_e2e = max(3, min(args.steps, 10))

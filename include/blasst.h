@@ -135,7 +135,8 @@ blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
  * Host-buffer call: blasst_attn_fwd on fixed-length tensors that live in HOST memory. The heads
  * are streamed through a caller-provided device workspace in groups of heads_per_group: the
  * host-to-device copies of one group overlap the kernel on the previous group and the
- * device-to-host copies of the group before that. (The attention of a head does not depend on
+ * device-to-host copies of the group before that; the kernels of consecutive groups run on
+ * two streams, so one can start while the other finishes. (The attention of a head does not depend on
  * any other head, so the outputs equal those of blasst_attn_fwd bit for bit.)
  *
  *   q            HOST [B, Sq, H, 128] bf16.   k, v   HOST [B, Sk, H, 128] bf16.
@@ -146,13 +147,13 @@ blasst_status blasst_attn_fwd_ex(const blasst_fwd_args *args);
  *                blasst_host_workspace_bytes(B, H, Sq, Sk, heads_per_group) bytes, owned by the
  *                caller; it must not be used by any other call until this one has completed.
  *   heads_per_group  1 .. H (H need not be a multiple of it): the largest group. Group sizes
- *                grow 1, 2, 4, ... up to it and the last group holds a single head, which
- *                shortens the pipeline's fill and drain.
+ *                grow 1, 2, 3, 5, 8, ... (about 1.5 times the previous) up to it and the last
+ *                group holds a single head, which shortens the pipeline's fill and drain.
  *   stream       the call starts after earlier work on `stream`, and work enqueued on `stream`
  *                afterwards starts after the last copy back: the host outputs are complete and the
  *                host inputs and the workspace free once `stream` reaches that point.
  *
- * The library owns two streams and seven events per device for this call, created at its first
+ * The library owns four streams and seven events per device for this call, created at its first
  * use on the device; calls on one device are enqueued one at a time (a library mutex). No
  * device memory is allocated. Per-head skip counts and the skip mask are not available here.
  * Same argument rules and return codes as blasst_attn_fwd; struct_size must be

@@ -310,7 +310,7 @@ def attn_fwd_host(q, k, v, factor: float, scale: float | None = None, *, out=Non
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if heads_per_group is None:
-        heads_per_group = max(1, (2 * H) // 5)
+        heads_per_group = max(1, H // 5)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned())
     if workspace is None:

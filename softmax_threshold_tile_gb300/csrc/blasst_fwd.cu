@@ -971,7 +971,7 @@ bool host_dims_ok(int B, int H, int Sq, int Sk, int hg) {
 // Streams and events of the host-buffer call, one set per device, made at its first use there.
 struct HostPipe {
   bool ready = false;
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp[2] = {};
   cudaEvent_t start = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
 };
 HostPipe g_pipe[kMaxDevices];
@@ -981,6 +981,8 @@ bool make_pipe(HostPipe& hp) {
   if (hp.ready) return true;
   bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.comp[0], cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.comp[1], cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < 2 && ok; ++i)
     ok = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming) == cudaSuccess &&
@@ -1022,13 +1024,18 @@ blasst_status launch_host(const blasst_host_args& a) {
   const size_t hrow = static_cast<size_t>(a.H) * kHeadDim * 2;  // host bytes per (batch, token)
   bool ok = cudaEventRecord(hp.start, cs) == cudaSuccess &&
             cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
-  // Groups of heads: sizes 1, 2, 4, ... up to hg, so that each group's copy-in is about as long
-  // as the previous group's kernel (a short pipeline fill), and a single head last (a short
-  // drain).
+            cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.comp[0], hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.comp[1], hp.start, 0) == cudaSuccess;
+  // Groups of heads: sizes 1, 2, 3, 5, 8, ... (about 1.5 times the previous) up to hg, so that
+  // each group's copy-in takes no longer than the previous group's kernel (a short pipeline
+  // fill), and a single head last (a short drain). The two workspace slots have a compute
+  // stream each, so the kernel of one group can start on the SMs that the previous group's
+  // kernel is leaving (no tail between launches).
   blasst_status kst = BLASST_OK;
   int want = 1;
-  for (int g = 0, h0 = 0, hc = 0; h0 < a.H && ok; ++g, h0 += hc, want = want * 2 < hg ? want * 2 : hg) {
+  for (int g = 0, h0 = 0, hc = 0; h0 < a.H && ok;
+       ++g, h0 += hc, want = want + (want + 1) / 2 < hg ? want + (want + 1) / 2 : hg) {
     const int rem = a.H - h0;
     hc = rem > want ? want : (rem > 1 && g > 0 ? rem - 1 : rem);
     const int s = g & 1;
@@ -1045,8 +1052,9 @@ blasst_status launch_host(const blasst_host_args& a) {
          cudaMemcpy2DAsync(base + slot.v, crow, static_cast<const uint8_t*>(a.v) + hoff, hrow, crow,
                            static_cast<size_t>(a.B) * a.Sk, cudaMemcpyHostToDevice, hp.in) == cudaSuccess &&
          cudaEventRecord(hp.in_done[s], hp.in) == cudaSuccess &&
-         cudaStreamWaitEvent(cs, hp.in_done[s], 0) == cudaSuccess;
-    if (ok && g >= 2) ok = cudaStreamWaitEvent(cs, hp.out_done[s], 0) == cudaSuccess;
+         cudaStreamWaitEvent(hp.comp[s], hp.in_done[s], 0) == cudaSuccess;
+    // The copy-out of group g - 2 read this slot's o and lse.
+    if (ok && g >= 2) ok = cudaStreamWaitEvent(hp.comp[s], hp.out_done[s], 0) == cudaSuccess;
     if (!ok) break;
     blasst_fwd_args fa{};
     fa.struct_size = sizeof(fa);
@@ -1062,10 +1070,10 @@ blasst_status launch_host(const blasst_host_args& a) {
     fa.d = a.d;
     fa.scale = a.scale;
     fa.factor = a.factor;
-    fa.stream = a.stream;
+    fa.stream = reinterpret_cast<struct CUstream_st*>(hp.comp[s]);
     kst = launch(fa);
     if (kst != BLASST_OK) break;
-    ok = cudaEventRecord(hp.comp_done[s], cs) == cudaSuccess &&
+    ok = cudaEventRecord(hp.comp_done[s], hp.comp[s]) == cudaSuccess &&
          cudaStreamWaitEvent(hp.out, hp.comp_done[s], 0) == cudaSuccess &&
          cudaMemcpy2DAsync(static_cast<uint8_t*>(a.o) + hoff, hrow, base + slot.o, crow, crow,
                            static_cast<size_t>(a.B) * a.Sq, cudaMemcpyDeviceToHost, hp.out) == cudaSuccess;

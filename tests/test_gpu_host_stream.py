@@ -23,6 +23,7 @@ def _gpu():
 
 @pytest.mark.parametrize("B,H,Sq,Sk,hg,pinned", [
     (2, 5, 1000, 777, 2, True), (1, 5, 1000, 777, 1, True), (2, 3, 300, 1300, 3, False), (1, 7, 129, 129, 4, True),
+    (1, 13, 700, 700, 5, True), (1, 20, 256, 300, 20, True),
 ])
 def test_host_call_equals_device_call(B, H, Sq, Sk, hg, pinned):
     import torch
