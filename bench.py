@@ -480,9 +480,15 @@ def run_ours(args, w):
         oracle.build()
         threads = min(os.cpu_count() or 1, args.cpu_units)
         rate, dt, units = cpu_oracle_rate(w, q, k, v, head_factor, args.cpu_units, threads)
+        # the same oracle on one core, on a smaller sample (query tiles are independent, so the
+        # rate does not depend on the sample's size)
+        n1 = max(1, min(4, args.cpu_units))
+        rate1, dt1, units1 = cpu_oracle_rate(w, q, k, v, head_factor, n1, 1)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{len(units)} query tiles (batch 0, heads 0 and {w.H - 1}, first tiles) of "
-                         f"{w.name} at factor {head_factor:g}; {dt:.1f} s wall"}
+                         f"{w.name} at factor {head_factor:g}; {dt:.1f} s wall",
+               "single_core": {"value": rate1, "unit": UNIT, "cores": 1,
+                               "sample": f"{len(units1)} query tiles of the same sample; {dt1:.1f} s wall"}}
 
     if rank == 0:
         line = {
