@@ -52,3 +52,23 @@ def test_host_call_equals_device_call(B, H, Sq, Sk, hg, pinned):
     o2, _ = blasst.attn_fwd_host(qh, kh, vh, 4.0, workspace=ws, heads_per_group=hg, stream=stream)
     stream.synchronize()
     assert torch.equal(o2, o)
+
+
+def test_host_call_at_factor_zero_equals_device_call():
+    """Factor 0 runs the lambda = 0 kernel instance inside the head-group pipeline."""
+    import torch
+    import softmax_threshold_tile_gb300 as blasst
+    B, H, Sq, Sk = 1, 6, 700, 900
+    q, k, v = parity.clustered_inputs(B, H, Sq, Sk, seed=77)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    ref = blasst.attn_fwd(qd, kd, vd, 0.0)
+    torch.cuda.synchronize()
+    qh, kh, vh = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for x in (q, k, v))
+    lse = torch.empty((B, H, Sq), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+    o, lse = blasst.attn_fwd_host(qh, kh, vh, 0.0, lse=lse, heads_per_group=3, stream=stream)
+    stream.synchronize()
+    assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
+    assert torch.equal(o, ref.o.cpu())
+    assert torch.equal(lse, ref.lse.cpu())
