@@ -110,3 +110,26 @@ def test_ragged_37000():
     units = parity.sample_units(w.B, w.H, w.S, heads=(0, 16, 31), qtiles=(0, 144, 289))
     stats = _run_workload_sweep(w, factors, units)
     assert stats[-1]["skip_fraction"] > 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(seed):
+    """Seeded random shapes (batch, heads, ragged Sq != Sk, clustering strength, factor), every
+    query tile checked against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 4))
+    H = int(rng.integers(1, 6))
+    Sq = int(rng.integers(1, 900))
+    Sk = int(rng.integers(1, 1400))
+    gamma = float(rng.uniform(0.0, 3.0))
+    factor = float(rng.choice([0.0, 0.25, 2.0, 16.0, 128.0]))
+    g = np.full(B * H, gamma)
+    q = synth.fill(1, B, Sq, H, 128, seed, (1, 1, Sq), (1, 1, 16), g)
+    k = synth.fill(2, B, Sk, H, 128, seed, (1, 1, Sk), (1, 1, 16), g)
+    v = synth.fill(3, B, Sk, H, 128, seed)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    o, lse, counts, mask = parity.run_gpu(qd, kd, vd, factor)
+    parity.check_counts(counts, mask, factor)
+    units = parity.sample_units(B, H, Sq, heads=range(H), qtiles=range(-(-Sq // 128)))
+    st = parity.compare_units(q, k, v, o, lse, mask, factor, units)
+    print(dict(B=B, H=H, Sq=Sq, Sk=Sk, gamma=round(gamma, 2), factor=factor), st)
