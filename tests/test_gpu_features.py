@@ -82,20 +82,26 @@ def _packed_to_device(q, k, v, cq, ck):
             torch.from_numpy(cq).cuda(), torch.from_numpy(ck).cuda())
 
 
-@pytest.mark.parametrize("factor", [0.0, 4.0, 64.0])
-def test_packed_documents_equal_separate_calls(factor):
+def _check_packed_equals_separate(lq, lk, factor, H=3, seed=5):
+    """Each document of a packed call equals the same document alone (bit for bit when the
+    decisions agree; lambda rounds differently through the float factor, so otherwise only
+    tiles within the decision margin may differ). Documents without keys return O = 0 and
+    lse = -inf; documents without queries write nothing."""
     import torch
-    lq = [1000, 37, 2048, 300, 129, 1]
-    lk = [1000, 37, 2048, 300, 129, 1]
-    q, k, v, cq, ck = _packed(lq, lk)
+    q, k, v, cq, ck = _packed(lq, lk, H=H, seed=seed)
     qd, kd, vd, cqd, ckd = _packed_to_device(q, k, v, cq, ck)
-    mq, mk = max(lq), max(lk)
+    mq, mk = max(max(lq), 1), max(max(lk), 1)
     res = _blasst().attn_varlen_fwd(qd, kd, vd, cqd, ckd, mq, mk, factor, want_max_prob=True)
     torch.cuda.synchronize()
     assert _clear_error() == 0
-    H = q.shape[1]
     counts = res.skip_counts.cpu().numpy().reshape(len(lq), H)
     for i, (a, b_) in enumerate(zip(lq, lk)):
+        if a == 0:
+            continue
+        if b_ == 0:
+            assert torch.count_nonzero(res.o[cq[i]:cq[i + 1]]) == 0
+            assert torch.all(torch.isinf(res.lse[:, cq[i]:cq[i + 1]]))
+            continue
         # the same document alone, with the factor that gives the same lambda = factor / max_seqlen_k
         fd = factor * b_ / mk
         qi, ki, vi = (t[None, s:e].contiguous() for t, s, e in ((qd, cq[i], cq[i + 1]), (kd, ck[i], ck[i + 1]), (vd, ck[i], ck[i + 1])))
@@ -107,15 +113,39 @@ def test_packed_documents_equal_separate_calls(factor):
             assert torch.equal(one.lse[0], res.lse[:, cq[i]:cq[i + 1]])
             assert torch.equal(one.max_prob[0], res.max_prob[:, cq[i]:cq[i + 1]])
         else:
-            # lambda rounds differently through the float factor: allow only marginal tiles
             m1 = one.skip_mask.cpu().numpy()
             ref = oracle.skip_softmax_attn(q[None, cq[i]:cq[i + 1]].copy(), k[None, ck[i]:ck[i + 1]].copy(),
                                            v[None, ck[i]:ck[i + 1]].copy(), 1 / math.sqrt(128), fd)
             gap = ref["gap"].reshape(m1.shape)
             lnlam = math.log(fd / b_) if fd > 0 else -math.inf
             assert np.all(np.abs(gap[m1.astype(bool) != (gap < lnlam)] - lnlam) < parity.MARGIN)
+    return counts
+
+
+@pytest.mark.parametrize("factor", [0.0, 4.0, 64.0])
+def test_packed_documents_equal_separate_calls(factor):
+    counts = _check_packed_equals_separate([1000, 37, 2048, 300, 129, 1], [1000, 37, 2048, 300, 129, 1], factor)
     if factor > 0:
         assert counts.sum() > 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_packed_documents(seed):
+    """Seeded random documents: 2 to 6 of them, lengths 0 ... 2100 (some empty, some of one
+    token), queries and keys of different lengths, 1 to 4 heads, a random factor."""
+    rng = np.random.default_rng(500 + seed)
+    n = int(rng.integers(2, 7))
+    lq = [int(x) for x in rng.choice([0, 1, 37, 128, 129, 700, 2100], size=n)]
+    lk = [int(x) if rng.random() < 0.5 else lq[i] for i, x in enumerate(rng.integers(0, 2100, size=n))]
+    lk = [max(x, 1) if lq[i] == 0 else x for i, x in enumerate(lk)]  # (a document needs queries or keys)
+    if sum(lq) == 0:
+        lq[0] = 64
+    if sum(lk) == 0:
+        lk[0] = 64
+    H = int(rng.integers(1, 5))
+    factor = float(rng.choice([0.0, 1.0, 8.0, 64.0]))
+    print(lq, lk, H, factor)
+    _check_packed_equals_separate(lq, lk, factor, H=H, seed=seed)
 
 
 def test_packed_documents_against_oracle():
