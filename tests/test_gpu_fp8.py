@@ -77,6 +77,21 @@ def test_fp8_ragged(Sq, Sk):
         s[0], s[2], s[1], heads=range(s[2]), qtiles=range(-(-s[1] // 128))), Sk)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_fp8_random_shapes(seed):
+    """Seeded random shapes for the e4m3 score product, every query tile checked."""
+    rng = np.random.default_rng(700 + seed)
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 5))
+    Sq, Sk = int(rng.integers(1, 900)), int(rng.integers(1, 1400))
+    gamma = float(rng.uniform(0.5, 3.0))
+    g = np.full(B * H, gamma)
+    q = synth.fill(1, B, Sq, H, 128, seed, (1, 1, Sq), (1, 1, 16), g)
+    k = synth.fill(2, B, Sk, H, 128, seed, (1, 1, Sk), (1, 1, 16), g)
+    v = synth.fill(3, B, Sk, H, 128, seed)
+    _check((q, k, v), [0.0, float(rng.choice([1.0, 8.0, 64.0]))], lambda s: parity.sample_units(
+        s[0], s[2], s[1], heads=range(s[2]), qtiles=range(-(-s[1] // 128))), Sk)
+
+
 def test_fp8_dit_8192_sampled():
     w = synth.WORKLOADS["dit_8192_g2"]
     st = _check(synth.make_qkv(w), [0.0, 16.0], lambda s: parity.sample_units(
