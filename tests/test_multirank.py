@@ -1,4 +1,4 @@
-"""The benchmark's multi-process path on CPU: two gloo ranks (one process per GPU on a GPU machine)
+"""The benchmark's multi-process path on CPU: two gloo ranks (one process per GPU on a multi-GPU machine)
 run the same barrier / max-over-ranks / weak-scaling aggregation the benchmark uses."""
 import os
 import socket
