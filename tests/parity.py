@@ -10,6 +10,7 @@ Tolerances (bf16 output O, per the parity bar of the method):
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 
@@ -66,10 +67,18 @@ def sample_units(B, H, Sq, heads=None, qtiles=None, batches=None):
                      dtype=np.int32)
 
 
-def compare_units(q, k, v, o_gpu, lse_gpu, mask_gpu, factor, units, scale=None, threads=16, margin=MARGIN):
+def host_threads():
+    """Every host core: the oracle's units are independent."""
+    return os.cpu_count() or 1
+
+
+def compare_units(q, k, v, o_gpu, lse_gpu, mask_gpu, factor, units, scale=None, threads=None, margin=MARGIN,
+                  return_gap=False):
     """Replay the GPU's decisions in the oracle on `units`; assert the parity bar.
 
-    Returns a dict of the observed errors and decision agreement."""
+    Returns a dict of the observed errors and decision agreement; with return_gap, its "gap"
+    entry holds the oracle's per-(unit, key tile) log margins max_i(tile_max - running_max)."""
+    threads = host_threads() if threads is None else threads
     B, Sq, H, d = q.shape
     Sk = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -98,8 +107,33 @@ def compare_units(q, k, v, o_gpu, lse_gpu, mask_gpu, factor, units, scale=None, 
     if factor / Sk <= 1.0:
         margins = np.abs(ref["gap"][differ] - ln_lam)
         assert np.all(margins < margin), f"decision differs on a tile with margin {margins.max():.3g}"
-    return {"max_abs": max_abs, "mean_abs": mean_abs, "lse_max_abs": float(lerr.max()),
-            "decisions": int(m_in.size), "differ": int(differ.sum()), "skipped": int(m_in.sum())}
+    out = {"max_abs": max_abs, "mean_abs": mean_abs, "lse_max_abs": float(lerr.max()),
+           "decisions": int(m_in.size), "differ": int(differ.sum()), "skipped": int(m_in.sum())}
+    if return_gap:
+        out["gap"] = ref["gap"]
+    return out
+
+
+def check_decisions(gap, mask, factor, Sk, margin=MARGIN):
+    """Decisions of a run at `factor` against the oracle's gap chain of the same units.
+
+    For lambda <= 1 a skipped tile never raises the running max, so the running max before key
+    tile j is the dense prefix max at every factor, and one oracle pass gives the gap of every
+    tile for all factors. The free-running decision is gap < ln(lambda); the GPU's may differ
+    only where |gap - ln(lambda)| < margin. Returns (decisions, differ)."""
+    assert factor / Sk <= 1.0
+    ln_lam = math.log(factor / Sk) if factor > 0 else -math.inf
+    free = gap < ln_lam
+    differ = free != mask.astype(bool)
+    if differ.any():
+        margins = np.abs(gap[differ] - ln_lam)
+        assert np.all(margins < margin), f"decision differs on a tile with margin {margins.max():.3g}"
+    return int(mask.size), int(differ.sum())
+
+
+def whole_head_units(b, h, Sq):
+    """Every query tile of one (batch, head)."""
+    return np.array([(b, h, t) for t in range(-(-Sq // TILE))], dtype=np.int32)
 
 
 def clustered_inputs(B, H, Sq, Sk, seed=0, gamma=2.0, cell=16):

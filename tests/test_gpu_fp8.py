@@ -141,8 +141,8 @@ def test_fp8_quantisation_error_is_the_oracles():
     r8 = blasst.attn_fwd(qd, kd, vd, 0.0, scale, q_descale=dq, k_descale=dk)
     torch.cuda.synchronize()
     units = parity.sample_units(w.B, w.H, w.S, heads=range(w.H), qtiles=(0, 3, 7))
-    ref16 = oracle.skip_softmax_attn(q, k, v, scale, 0.0, units=units, threads=16)
-    ref8 = oracle.skip_softmax_attn(qo, ko, v, oscale, 0.0, units=units, threads=16)
+    ref16 = oracle.skip_softmax_attn(q, k, v, scale, 0.0, units=units, threads=parity.host_threads())
+    ref8 = oracle.skip_softmax_attn(qo, ko, v, oscale, 0.0, units=units, threads=parity.host_threads())
     o8 = r8.o.float().cpu().numpy()
     got = np.stack([o8[b, t * 128:(t + 1) * 128, h] for b, h, t in units])
     quant = np.abs(ref8["o"] - ref16["o"])
