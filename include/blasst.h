@@ -29,6 +29,7 @@
 #ifndef BLASST_H_
 #define BLASST_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -106,8 +107,16 @@ blasst_status blasst_attn_fwd(const void *q, const void *k, const void *v, void 
  *                 "video-attention" blog (section "First, the hardware ceiling") notes that the
  *                 two products cost the same and only the score product tolerates the low
  *                 precision there; the score product is the part skipping never removes.
+ *   status        DEVICE uint32 word or NULL, owned by the caller: zeroed on `stream` by the
+ *                 call, then OR-ed with the error bits of every CTA whose bounded wait gave up
+ *                 (1 producer, 2 MMA issuer, 4 softmax warps, 8 exit drain) or whose
+ *                 packed-document offsets were invalid (16). A stream-ordered copy of it after the
+ *                 call tells the caller whether o / lse are complete, without synchronizing the
+ *                 device (blasst_device_error reports the same bits device-wide).
  *
- * struct_size must be sizeof(blasst_fwd_args). Same return codes as blasst_attn_fwd.
+ * struct_size must be sizeof(blasst_fwd_args); the size of the layout without `status` (the
+ * offset of that member) is also accepted, with status taken as NULL. Same return codes as
+ * blasst_attn_fwd.
  */
 typedef struct blasst_fwd_args {
   uint32_t struct_size;
@@ -125,6 +134,7 @@ typedef struct blasst_fwd_args {
   int min_seq_len;
   int qk_format;
   float q_descale, k_descale;
+  uint32_t *status;
 } blasst_fwd_args;
 
 enum { BLASST_QK_BF16 = 0, BLASST_QK_E4M3 = 1 };
@@ -228,6 +238,22 @@ blasst_status blasst_flow_shift_schedule(double shift, int num_points, double *t
 
 /* Library version as major * 10000 + minor * 100 + patch. */
 int blasst_version(void);
+
+/*
+ * Test hook for the bounded device waits (no counterpart in the method): from the next call
+ * on, in every process-wide kernel launch, the TMA producer never issues the copy of key tile
+ * `tile`, so the waits on it run out after their time limit, the CTAs leave through their
+ * abort path and the error bits show in `status` and blasst_device_error. -1 (the initial
+ * state) switches it off. Returns BLASST_ERR_INVALID_ARG for tile < -1.
+ */
+blasst_status blasst_debug_withhold_key_tile(int tile);
+
+/*
+ * Number of TMA tensor descriptors this process has encoded so far. Each call needs one for
+ * q, k and v; they are kept in a small per-process cache keyed by (address, shape, format),
+ * so repeated calls on the same tensors encode none.
+ */
+uint64_t blasst_tensor_map_encodes(void);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,9 @@ from ._binding import (  # noqa: F401
     attn_fwd_host,
     host_workspace,
     blasst_attn_fwd_host,
+    blasst_debug_withhold_key_tile,
     blasst_host_workspace_bytes,
+    blasst_tensor_map_encodes,
     attn_varlen_fwd,
     blasst_attn_fwd_ex,
     blasst_attn_fwd,

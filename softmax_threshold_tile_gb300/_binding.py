@@ -43,6 +43,7 @@ class FwdArgs(ctypes.Structure):
         ("min_seq_len", ctypes.c_int),
         ("qk_format", ctypes.c_int),
         ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
+        ("status", ctypes.c_void_p),
     ]
 
 
@@ -97,6 +98,10 @@ def load_library(path: str | None = None):
     lib.blasst_device_error.argtypes = [u32p, ctypes.c_int]
     lib.blasst_version.restype = ctypes.c_int
     lib.blasst_version.argtypes = []
+    lib.blasst_debug_withhold_key_tile.restype = ctypes.c_int
+    lib.blasst_debug_withhold_key_tile.argtypes = [ctypes.c_int]
+    lib.blasst_tensor_map_encodes.restype = ctypes.c_uint64
+    lib.blasst_tensor_map_encodes.argtypes = []
     dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
     lib.blasst_factor_from_threshold.restype = ctypes.c_int
     lib.blasst_factor_from_threshold.argtypes = [ctypes.c_double, ctypes.c_int64, dp]
@@ -132,7 +137,8 @@ def blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream, ski
 
 def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor, stream, skip_counts,
                        skip_mask_dbg, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0,
-                       min_seq_len=0, qk_format=BLASST_QK_BF16, q_descale=1.0, k_descale=1.0) -> int:
+                       min_seq_len=0, qk_format=BLASST_QK_BF16, q_descale=1.0, k_descale=1.0,
+                       status=None) -> int:
     """The extended C entry point: fills a ``blasst_fwd_args`` and calls it."""
     a = FwdArgs()
     a.struct_size = ctypes.sizeof(FwdArgs)
@@ -144,6 +150,7 @@ def blasst_attn_fwd_ex(q, k, v, o, lse, max_prob, B, H, Sq, Sk, d, scale, factor
     a.cu_seqlens_q, a.cu_seqlens_k = _p(cu_seqlens_q), _p(cu_seqlens_k)
     a.max_seqlen_q, a.max_seqlen_k, a.min_seq_len = int(max_seqlen_q), int(max_seqlen_k), int(min_seq_len)
     a.qk_format, a.q_descale, a.k_descale = int(qk_format), float(q_descale), float(k_descale)
+    a.status = _p(status)
     return int(load_library().blasst_attn_fwd_ex(ctypes.byref(a)))
 
 
@@ -164,6 +171,17 @@ def blasst_attn_fwd_host(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, worksp
     a.heads_per_group = int(heads_per_group)
     a.stream = _p(stream)
     return int(load_library().blasst_attn_fwd_host(ctypes.byref(a)))
+
+
+def blasst_debug_withhold_key_tile(tile: int) -> int:
+    """Test hook of the bounded device waits: the producer withholds the copy of key tile `tile`
+    in every launch from now on (-1: off)."""
+    return int(load_library().blasst_debug_withhold_key_tile(int(tile)))
+
+
+def blasst_tensor_map_encodes() -> int:
+    """TMA tensor descriptors encoded by this process so far (the cache's misses)."""
+    return int(load_library().blasst_tensor_map_encodes())
 
 
 def blasst_status_string(code: int) -> str:
@@ -217,12 +235,14 @@ def _check_qkv(q, k, v, packed: bool) -> int:
 def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, want_lse: bool = True,
              want_counts: bool = True, want_mask: bool = False, want_max_prob: bool = False,
              min_seq_len: int = 0, q_descale: float = 1.0, k_descale: float = 1.0,
-             stream=None) -> AttnResult:
+             status=None, stream=None) -> AttnResult:
     """Skip-Softmax attention on torch CUDA tensors [B, S, H, 128] (contiguous): q / k / v bf16,
     or q / k float8_e4m3fn with v bf16 (scores then carry q_descale * k_descale).
 
     Allocates the outputs with torch (device memory only) and calls the C entry point on the
-    current (or given) stream. Raises BlasstError on any non-OK status.
+    current (or given) stream. `status` (optional CUDA int32 tensor of one element) receives the
+    error bits of CTAs whose device waits gave up, zeroed by the call first. Raises BlasstError on
+    any non-OK status.
     """
     import torch
 
@@ -240,12 +260,12 @@ def attn_fwd(q, k, v, factor: float, scale: float | None = None, *, out=None, wa
     mask = torch.empty((B, H, nQ, nK), dtype=torch.uint8, device=dev) if want_mask else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    if mp is None and min_seq_len == 0 and qk_format == BLASST_QK_BF16:
+    if mp is None and min_seq_len == 0 and qk_format == BLASST_QK_BF16 and status is None:
         st = blasst_attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts, mask)
     else:
         st = blasst_attn_fwd_ex(q, k, v, o, lse, mp, B, H, Sq, Sk, d, scale, factor, stream.cuda_stream, counts,
                                 mask, min_seq_len=min_seq_len, qk_format=qk_format, q_descale=q_descale,
-                                k_descale=k_descale)
+                                k_descale=k_descale, status=status)
     if st != BLASST_OK:
         raise BlasstError(st, "blasst_attn_fwd")
     return AttnResult(o, lse, counts, mask, mp)
@@ -313,10 +333,13 @@ def attn_fwd_host(q, k, v, factor: float, scale: float | None = None, *, out=Non
         heads_per_group = max(1, H // 5)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned())
-    if workspace is None:
-        workspace = host_workspace(B, H, Sq, Sk, heads_per_group)
     if stream is None:
         stream = torch.cuda.current_stream()
+    if workspace is None:
+        # Allocated on `stream`, the stream the call's last step joins: once this tensor is
+        # released, the caching allocator hands its block only to work ordered after the call.
+        with torch.cuda.stream(stream):
+            workspace = host_workspace(B, H, Sq, Sk, heads_per_group)
     st = blasst_attn_fwd_host(q, k, v, out, lse, B, H, Sq, Sk, d, scale, factor, workspace,
                               workspace.numel() * workspace.element_size(), heads_per_group, stream.cuda_stream)
     if st != BLASST_OK:

@@ -40,9 +40,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -107,6 +108,7 @@ struct alignas(1024) Smem {
   float hmax[kQTiles][2][kTile];   // half-row maxima of the current key tile (tile, half, row)
   float lpart[kQTiles][2][kTile];  // half-row sums at the end (tile, half, row)
   uint32_t abort;             // some role gave up waiting
+  uint32_t* status;           // the caller's device status word, or null
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base to 1024 B
 
@@ -124,7 +126,14 @@ struct FwdParams {
   int Tq, Tk;         // varlen: total query / key tokens (token extents of the packed tensors)
   int min_seq_len;    // documents with fewer keys than this run dense
   int withhold_k;     // test of the bounded waits: the copy of this key tile is never issued (-1: off)
+  uint32_t* status;   // the caller's device status word, or null
 };
+
+// Error bits go to the device-wide word and, when the caller passed one, to its status word.
+__device__ __forceinline__ void report_error(uint32_t* status, uint32_t bits) {
+  atomicOr(&g_error_word, bits);
+  if (status) atomicOr(status, bits);
+}
 
 // What one CTA works on: one batch entry (or packed document) and head, and its lengths.
 struct Geo {
@@ -173,7 +182,7 @@ __device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
     g.Sq = min(max(q1, g.q_tok0), p.Tq) - g.q_tok0;
     g.Sk = min(max(k1, g.k_tok0), p.Tk) - g.k_tok0;
     if (q0 < 0 || k0 < 0 || q1 < q0 || k1 < k0 || q1 > p.Tq || k1 > p.Tk || g.Sq > p.Sq || g.Sk > p.Sk) {
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_error_word, kErrGeometry);
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) report_error(p.status, kErrGeometry);
       g.Sq = min(g.Sq, p.Sq);
       g.Sk = min(g.Sk, p.Sk);
     }
@@ -201,10 +210,10 @@ __device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
 // Bounded wait on an mbarrier phase. Gives up after `timeout_ns`, or at once when
 // another role has given up (unless `respect_abort` is false); on a timeout it
 // records `site` in the device error word and raises the CTA abort flag.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
-                                         uint32_t site, bool respect_abort = true,
-                                         uint64_t timeout_ns = kWaitTimeoutNs) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem& sm, uint32_t site,
+                                         bool respect_abort = true, uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
+  volatile uint32_t* abort = &sm.abort;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -212,7 +221,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       if (respect_abort && *abort) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
         *abort = 1u;
-        atomicOr(&g_error_word, site);
+        report_error(sm.status, site);
         return false;
       }
     }
@@ -232,7 +241,6 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
                                              const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
                                              int qt0) {
   const Lens<kVarlen> L{p, g};
-  volatile uint32_t* abort = &sm.abort;
   prefetch_tmap(tq);
   prefetch_tmap(tk);
   prefetch_tmap(tv);
@@ -283,11 +291,13 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     // lambda = 0: every key tile is kept, so no decision is waited for. K_(j+1) and V_j go out
     // together, and the stages are released by the scores instead: S_B(j) is committed after
     // every MMA up to Q_B K_j^T, which covers the readers of K_j and of V_(j-1), the tiles the
-    // next iteration's copies overwrite.
+    // next iteration's copies overwrite. The softmax warps report that they saw S_B(j) on
+    // dec[B][j % 2]: each slot is waited once per use, and its next phase (key tile j + 2)
+    // needs K_(j+2), which is issued only after this wait, so the parity cannot alias.
     for (int j = 0; j < L.nK() && ok; ++j) {
       if (j + 1 < L.nK()) issue_k(j + 1);
       issue_v(j);
-      ok = wait_bar(smem_u32(&sm.s_full[kQTiles - 1]), j & 1, abort, kErrProducer);
+      ok = wait_bar(smem_u32(&sm.dec[kQTiles - 1][j & 1]), (j >> 1) & 1, sm, kErrProducer);
     }
   }
   for (int j = 0; j < L.nK() && ok && !kDense; ++j) {
@@ -298,7 +308,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     bool loaded = false;
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {
-      if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, abort, kErrProducer)) { ok = false; break; }
+      if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, sm, kErrProducer)) { ok = false; break; }
       const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
       if (!skip && !loaded) {
         issue_v(j);
@@ -311,18 +321,17 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   for (int back = 1; back <= kStages; ++back) {
     const int nk = k_issued - back, nv = v_issued - back;
     if (nk >= 0)
-      wait_bar(smem_u32(&sm.k_full[nk & 1]), (nk >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
+      wait_bar(smem_u32(&sm.k_full[nk & 1]), (nk >> 1) & 1, sm, kErrDrain, false, kDrainTimeoutNs);
     if (nv >= 0)
-      wait_bar(smem_u32(&sm.v_full[nv & 1]), (nv >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
+      wait_bar(smem_u32(&sm.v_full[nv & 1]), (nv >> 1) & 1, sm, kErrDrain, false, kDrainTimeoutNs);
   }
-  wait_bar(q_full, 0, abort, kErrDrain, false, kDrainTimeoutNs);
+  wait_bar(q_full, 0, sm, kErrDrain, false, kDrainTimeoutNs);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 template <bool kVarlen, bool kFp8, bool kDense>
 __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
   const Lens<kVarlen> L{p, g};
-  volatile uint32_t* abort = &sm.abort;
   constexpr uint32_t kIdescQK = kFp8 ? idesc_e4m3_f32(kTile, kTile)          // K tile is K-major
                                      : idesc_bf16_f32(kTile, kTile, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
@@ -377,8 +386,8 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   };
 
   int pv_issued0 = 0, pv_issued1 = 0;
-  bool ok = wait_bar(smem_u32(&sm.q_full), 0, abort, kErrMma) &&
-            wait_bar(smem_u32(&sm.k_full[0]), 0, abort, kErrMma);
+  bool ok = wait_bar(smem_u32(&sm.q_full), 0, sm, kErrMma) &&
+            wait_bar(smem_u32(&sm.k_full[0]), 0, sm, kErrMma);
   if (ok) {
     tc_fence_after();
 #pragma unroll
@@ -398,13 +407,13 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
       for (int t = 0; t < kQTiles; ++t) {
         // p_ready arrives once the tile has read S_t and decided: at once for a skipped
         // key tile, after P is written (and O rescaled) for a kept one.
-        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
+        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, sm, kErrMma)) { ok = false; break; }
         tc_fence_after();
         // (lambda = 0 keeps every key tile: no decision to read.)
         const uint32_t skip = kDense ? 0u : *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
         if (!skip) {
           if (!v_ready) {
-            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
+            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, sm, kErrMma)) { ok = false; break; }
             tc_fence_after();
             v_ready = true;
           }
@@ -416,7 +425,7 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
           // S_t is free: it was read before p_ready, and its P (if the tile was kept) is
           // read by the P V just issued; tcgen05.mma executes in issue order.
           if (t == 0) {
-            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, abort, kErrMma)) { ok = false; break; }
+            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, sm, kErrMma)) { ok = false; break; }
             tc_fence_after();
           }
           issue_qk(t, nst);
@@ -435,7 +444,7 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   for (int t = 0; t < kQTiles; ++t) tc_commit(smem_u32(&sm.o_done[t]));
   // Every MMA this thread issued completes before TMEM is released.
   tc_commit(smem_u32(&sm.drain));
-  wait_bar(smem_u32(&sm.drain), 0, abort, kErrDrain, false, kDrainTimeoutNs);
+  wait_bar(smem_u32(&sm.drain), 0, sm, kErrDrain, false, kDrainTimeoutNs);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -462,7 +471,6 @@ template <bool kVarlen, bool kMaxProb, bool kDense>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
                                             int b, int h, int qt0) {
   const Lens<kVarlen> L{p, g};
-  volatile uint32_t* abort = &sm.abort;
   const int warp = threadIdx.x >> 5;
   const int wq = warp & 3;                // TMEM lane quarter
   const int half = warp >> 2;             // key columns 64 * half ... + 63; O features likewise
@@ -485,8 +493,10 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     float hmax = -INFINITY;
     uint32_t sr[64];
     if (!failed) {
-      const bool ok = wait_bar(smem_u32(&sm.s_full[t]), j & 1, abort, kErrSoftmax);
+      const bool ok = wait_bar(smem_u32(&sm.s_full[t]), j & 1, sm, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
+      // lambda = 0: tell the producer that S_B(j) has completed (it reuses the stages then).
+      if (kDense && t == kQTiles - 1 && leader && !failed) mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
     }
     if (!failed) {
       tc_fence_after();
@@ -605,8 +615,8 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   sm.lpart[0][half][row] = cur.l;
   sm.lpart[1][half][row] = oth.l;
   bar_sync_n<2 * kSoftmaxThreads>(3u);
-  const bool ok = failed ? false : wait_bar(smem_u32(&sm.o_done[0]), 0, abort, kErrSoftmax) &&
-                                       wait_bar(smem_u32(&sm.o_done[1]), 0, abort, kErrSoftmax);
+  const bool ok = failed ? false : wait_bar(smem_u32(&sm.o_done[0]), 0, sm, kErrSoftmax) &&
+                                       wait_bar(smem_u32(&sm.o_done[1]), 0, sm, kErrSoftmax);
   if (!__all_sync(0xffffffffu, ok)) return;
   tc_fence_after();
 #pragma unroll 1
@@ -699,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0u;
+    sm.status = p.status;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -773,6 +784,49 @@ bool encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, bool e
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// Tensor descriptors are a pure function of (address, shape, format), so a small per-process
+// table keeps the last ones encoded and repeated calls on the same tensors encode nothing.
+struct TmapKey {
+  const void* base;
+  int B, S, H;
+  bool e4m3;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && B == o.B && S == o.S && H == o.H && e4m3 == o.e4m3;
+  }
+};
+constexpr int kTmapCacheSize = 48;
+struct TmapCache {
+  std::mutex mutex;
+  TmapKey key[kTmapCacheSize] = {};
+  CUtensorMap map[kTmapCacheSize];
+  bool used[kTmapCacheSize] = {};
+  int next = 0;
+};
+TmapCache g_tmaps;
+std::atomic<uint64_t> g_tmap_encodes{0};
+
+bool cached_bshd(CUtensorMap* map, const void* base, int B, int S, int H, bool e4m3) {
+  const TmapKey key{base, B, S, H, e4m3};
+  std::lock_guard<std::mutex> lock(g_tmaps.mutex);
+  for (int i = 0; i < kTmapCacheSize; ++i) {
+    if (g_tmaps.used[i] && g_tmaps.key[i] == key) {
+      *map = g_tmaps.map[i];
+      return true;
+    }
+  }
+  if (!encode_bshd(map, base, B, S, H, e4m3)) return false;
+  g_tmap_encodes.fetch_add(1, std::memory_order_relaxed);
+  const int slot = g_tmaps.next;
+  g_tmaps.next = (slot + 1) % kTmapCacheSize;
+  g_tmaps.key[slot] = key;
+  g_tmaps.map[slot] = *map;
+  g_tmaps.used[slot] = true;
+  return true;
+}
+
+// The key tile whose copy the producer withholds (test of the bounded waits; -1: off).
+std::atomic<int> g_withhold_k{-1};
 
 // The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K,
 // 8 = lambda = 0 with bf16 scores; e4m3 scores at lambda = 0 run the general instance, which
@@ -864,6 +918,7 @@ blasst_status launch(const blasst_fwd_args& a) {
   if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.o, 16))
     return BLASST_ERR_INVALID_ARG;
   if ((a.lse && !aligned(a.lse, 4)) || (a.max_prob && !aligned(a.max_prob, 4))) return BLASST_ERR_INVALID_ARG;
+  if (a.status && !aligned(a.status, 4)) return BLASST_ERR_INVALID_ARG;
   if (a.min_seq_len < 0) return BLASST_ERR_INVALID_ARG;
   if (varlen) {
     if (!a.cu_seqlens_q || !a.cu_seqlens_k || !aligned(a.cu_seqlens_q, 4) || !aligned(a.cu_seqlens_k, 4))
@@ -882,8 +937,8 @@ blasst_status launch(const blasst_fwd_args& a) {
   // Fixed length: [B, S, H, 128] views. Packed documents: one [1, T, H, 128] view of all tokens.
   const int tb = varlen ? 1 : a.B;
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, a.q, tb, a.Sq, a.H, e4m3) || !encode_bshd(&tk, a.k, tb, a.Sk, a.H, e4m3) ||
-      !encode_bshd(&tv, a.v, tb, a.Sk, a.H))
+  if (!cached_bshd(&tq, a.q, tb, a.Sq, a.H, e4m3) || !cached_bshd(&tk, a.k, tb, a.Sk, a.H, e4m3) ||
+      !cached_bshd(&tv, a.v, tb, a.Sk, a.H, false))
     return BLASST_ERR_LAUNCH;
 
   FwdParams p{};
@@ -907,19 +962,18 @@ blasst_status launch(const blasst_fwd_args& a) {
   p.Tq = a.Sq;
   p.Tk = a.Sk;
   p.min_seq_len = a.min_seq_len;
-  // Test switch for the bounded device waits: BLASST_TEST_WITHHOLD_K_TILE=j makes the producer
-  // skip the copy of key tile j, so the waits on it give up after their time limit, the CTA
-  // leaves through its abort path and blasst_device_error reports the role. Off when unset.
-  p.withhold_k = -1;
-  if (const char* w = std::getenv("BLASST_TEST_WITHHOLD_K_TILE")) {
-    char* end = nullptr;
-    const long v = std::strtol(w, &end, 10);
-    if (end != w && v >= 0 && v < 0x7fffffffL) p.withhold_k = static_cast<int>(v);
-  }
+  // Test of the bounded device waits (blasst_debug_withhold_key_tile): the producer skips the
+  // copy of this key tile, so the waits on it give up after their time limit.
+  p.withhold_k = g_withhold_k.load(std::memory_order_relaxed);
+  p.status = a.status;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
   if (a.skip_counts &&
       cudaMemsetAsync(a.skip_counts, 0, sizeof(uint32_t) * static_cast<size_t>(a.B) * a.H, st) != cudaSuccess) {
+    cudaGetLastError();
+    return BLASST_ERR_LAUNCH;
+  }
+  if (a.status && cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st) != cudaSuccess) {
     cudaGetLastError();
     return BLASST_ERR_LAUNCH;
   }
@@ -1096,6 +1150,7 @@ blasst_status launch_host(const blasst_host_args& a) {
 }
 
 }  // namespace
+
 }  // namespace blasst
 
 extern "C" size_t blasst_host_workspace_bytes(int B, int H, int Sq, int Sk, int heads_per_group) {
@@ -1133,7 +1188,15 @@ extern "C" blasst_status blasst_attn_fwd(const void* q, const void* k, const voi
 }
 
 extern "C" blasst_status blasst_attn_fwd_ex(const blasst_fwd_args* args) {
-  if (!args || args->struct_size != sizeof(blasst_fwd_args)) return BLASST_ERR_INVALID_ARG;
+  if (!args) return BLASST_ERR_INVALID_ARG;
+  if (args->struct_size == offsetof(blasst_fwd_args, status)) {
+    // the layout before the status word: copy what the caller has, status NULL
+    blasst_fwd_args a{};
+    std::memcpy(&a, args, offsetof(blasst_fwd_args, status));
+    a.status = nullptr;
+    return blasst::launch(a);
+  }
+  if (args->struct_size != sizeof(blasst_fwd_args)) return BLASST_ERR_INVALID_ARG;
   return blasst::launch(*args);
 }
 
@@ -1170,4 +1233,14 @@ extern "C" blasst_status blasst_device_error(uint32_t* word, int clear) {
   return w ? BLASST_ERR_TIMEOUT : BLASST_OK;
 }
 
-extern "C" int blasst_version(void) { return 10200; }
+extern "C" int blasst_version(void) { return 10300; }
+
+extern "C" blasst_status blasst_debug_withhold_key_tile(int tile) {
+  if (tile < -1) return BLASST_ERR_INVALID_ARG;
+  blasst::g_withhold_k.store(tile, std::memory_order_relaxed);
+  return BLASST_OK;
+}
+
+extern "C" uint64_t blasst_tensor_map_encodes(void) {
+  return blasst::g_tmap_encodes.load(std::memory_order_relaxed);
+}

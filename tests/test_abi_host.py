@@ -125,6 +125,7 @@ def call_ex(**kw):
     dict(qk_format=1, q_descale=0.0), dict(qk_format=1, k_descale=-2.0),
     dict(qk_format=1, q_descale=float("nan")), dict(qk_format=1, k_descale=float("inf")),
     dict(qk_format=1, q=264),                               # e4m3 q must still be 16-byte aligned
+    dict(status=4098),                                      # the status word must be 4-byte aligned
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_extended_invalid_arguments(lib, kw):
     assert call_ex(**kw) == blasst.BLASST_ERR_INVALID_ARG
@@ -136,6 +137,30 @@ def test_extended_rejects_wrong_struct_size(lib):
     a.struct_size = ctypes.sizeof(blasst.FwdArgs) - 4
     assert lib.blasst_attn_fwd_ex(ctypes.byref(a)) == blasst.BLASST_ERR_INVALID_ARG
     assert lib.blasst_attn_fwd_ex(None) == blasst.BLASST_ERR_INVALID_ARG
+
+
+def test_extended_accepts_the_layout_without_status(lib):
+    """A caller built against the layout before the status word passes that smaller struct_size:
+    its arguments are read (an invalid one is still rejected) and status counts as NULL."""
+    import ctypes
+    old = blasst.FwdArgs.status.offset
+    a = blasst.FwdArgs()
+    a.struct_size = old
+    a.q, a.k, a.v, a.o = 256, 512, 768, 1024
+    a.B, a.H, a.Sq, a.Sk, a.d = 1, 2, 300, 300, 128
+    a.scale, a.factor = 1 / math.sqrt(128), 2.0
+    a.status = 4098  # past the caller's struct: never read
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert lib.blasst_attn_fwd_ex(ctypes.byref(a)) == blasst.BLASST_ERR_UNSUPPORTED_DEVICE
+    a.d = 64
+    assert lib.blasst_attn_fwd_ex(ctypes.byref(a)) == blasst.BLASST_ERR_INVALID_ARG
+
+
+def test_debug_hooks(lib):
+    assert blasst.blasst_debug_withhold_key_tile(-2) == blasst.BLASST_ERR_INVALID_ARG
+    assert blasst.blasst_debug_withhold_key_tile(-1) == blasst.BLASST_OK
+    assert blasst.blasst_tensor_map_encodes() >= 0
 
 
 def test_host_args_struct_matches_header(tmp_path):

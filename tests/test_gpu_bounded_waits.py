@@ -1,9 +1,11 @@
 """GPU test of failure detection: a device-side wait that runs out gives up, the kernel
-leaves through its abort path, the host reads the error word, and the context stays usable.
+leaves through its abort path, the caller reads the failure from its own status word (a
+stream-ordered copy, no device-wide synchronization) and from the device error word, and the
+context stays usable.
 
-The failure is made by a test switch (environment variable BLASST_TEST_WITHHOLD_K_TILE)
-under which the producer never issues the copy of one key tile, so the waits on it run
-out after their time limit. Nothing faults: every device wait in the kernel is bounded."""
+The failure is made by the library's test hook blasst_debug_withhold_key_tile, under which the
+producer never issues the copy of one key tile, so the waits on it run out after their time
+limit. Nothing faults: every device wait in the kernel is bounded."""
 import time
 
 import numpy as np
@@ -33,28 +35,41 @@ def _gpu():
 
 @pytest.mark.parametrize("factor", [2.0, 0.0])   # the general instance and the lambda = 0 one
 @pytest.mark.parametrize("tile", [0, 1, 3])
-def test_withheld_key_tile_times_out_and_context_survives(monkeypatch, tile, factor):
+def test_withheld_key_tile_times_out_and_context_survives(tile, factor):
     import torch
     import softmax_threshold_tile_gb300 as blasst
     q, k, v = parity.clustered_inputs(1, 2, 512, 512, seed=7)
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
-    ref = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True)
-    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    status = torch.full((1,), 0x55, dtype=torch.int32, device="cuda")
+    ref = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True, status=status, stream=stream)
+    stream.synchronize()
+    assert int(status.item()) == 0          # zeroed by the call, no wait gave up
     assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
 
-    monkeypatch.setenv("BLASST_TEST_WITHHOLD_K_TILE", str(tile))
-    t0 = time.monotonic()
-    blasst.attn_fwd(qd, kd, vd, factor)        # enqueued: the failure shows on the device
+    assert blasst.blasst_debug_withhold_key_tile(tile) == blasst.BLASST_OK
+    try:
+        t0 = time.monotonic()
+        blasst.attn_fwd(qd, kd, vd, factor, status=status, stream=stream)  # the failure shows on the device
+        host_status = torch.empty(1, dtype=torch.int32).pin_memory()
+        with torch.cuda.stream(stream):
+            host_status.copy_(status, non_blocking=True)            # ordered after the kernel on its stream
+        stream.synchronize()
+        elapsed = time.monotonic() - t0
+    finally:
+        assert blasst.blasst_debug_withhold_key_tile(-1) == blasst.BLASST_OK
+    word_s = int(host_status.item())
+    assert word_s & ERR_ROLES, f"status word {word_s:#x}"
+    assert (word_s & ~0x1f) == 0, f"status word {word_s:#x}"
     st, word = blasst.blasst_device_error(clear=True)
-    elapsed = time.monotonic() - t0
-    monkeypatch.delenv("BLASST_TEST_WITHHOLD_K_TILE")
     assert st == blasst.BLASST_ERR_TIMEOUT
     assert word & ERR_ROLES, f"error word {word:#x}"
     assert (word & ~0x1f) == 0, f"error word {word:#x}"
     assert elapsed < 20.0
 
-    again = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True)
-    torch.cuda.synchronize()
+    again = blasst.attn_fwd(qd, kd, vd, factor, want_mask=True, status=status, stream=stream)
+    stream.synchronize()
+    assert int(status.item()) == 0          # the next call is clean
     assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
     assert torch.equal(again.o, ref.o) and torch.equal(again.lse, ref.lse)
     np.testing.assert_array_equal(again.skip_mask.cpu().numpy(), ref.skip_mask.cpu().numpy())

@@ -72,3 +72,28 @@ def test_host_call_at_factor_zero_equals_device_call():
     assert blasst.blasst_device_error(clear=True) == (blasst.BLASST_OK, 0)
     assert torch.equal(o, ref.o.cpu())
     assert torch.equal(lse, ref.lse.cpu())
+
+
+def test_default_workspace_outlives_the_call_on_another_stream():
+    """Without a caller workspace the binding allocates one on the call's stream and drops it at
+    once; work that the caller then allocates and writes on its current (different) stream must
+    not receive that block while the call's copies and kernels still use it."""
+    import torch
+    import softmax_threshold_tile_gb300 as blasst
+    B, H, Sq, Sk, hg = 1, 6, 900, 900, 2
+    q, k, v = parity.clustered_inputs(B, H, Sq, Sk, seed=31)
+    qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
+    ref = blasst.attn_fwd(qd, kd, vd, 4.0)
+    torch.cuda.synchronize()
+    qh, kh, vh = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for x in (q, k, v))
+    ws_bytes = blasst.blasst_host_workspace_bytes(B, H, Sq, Sk, hg)
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        o, _ = blasst.attn_fwd_host(qh, kh, vh, 4.0, heads_per_group=hg, stream=side)
+        junk = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")   # on the current stream
+        junk.fill_(0xFF)
+        side.synchronize()
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref.o.cpu())
+        del junk
