@@ -217,10 +217,34 @@ def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
     return world * units_per_rank / (ms_max * 1e-3)
 
 
-def cpu_oracle_rate(w, q, k, v, factor, n_units, threads):
-    """Dense-equivalent TFLOPS of the CPU oracle on a bounded sample of query tiles."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_oracle_rate(w, q, k, v, factor, n_units, threads, units=None):
+    """Dense-equivalent TFLOPS of the CPU oracle on a bounded sample of query tiles (all query
+    tiles of the workload when `units` is "all")."""
     import oracle
-    units = sample_units(w, n_units)
+    if units is None:
+        units = sample_units(w, n_units)
+    elif isinstance(units, str):
+        units = oracle.all_units(w.B, w.H, w.S)
     scale = 1.0 / math.sqrt(w.d)
     t0 = time.perf_counter()
     oracle.skip_softmax_attn(q, k, v, scale, factor, units=units, threads=threads)
@@ -253,7 +277,8 @@ def run_reference(args, w):
     flops = sum(4.0 * min(TILE, w.S - TILE * int(t)) * w.S * w.d for _, _, t in units)
     value = flops * args.steps / sum(times) / 1e12
     sample = (f"{len(units)} query tiles of {w.name} (batch 0, heads 0 and {w.H - 1}, first tiles) "
-              f"per step at factor {factor:g}, fp64 scalar C oracle")
+              f"per step at factor {factor:g}, fp64 scalar C oracle; rate extrapolated to the whole "
+              f"call from {len(units)} of {w.B * w.H * (-(-w.S // TILE))} query tiles")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
@@ -261,7 +286,8 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded clustered video-DiT token grid)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "d": w.d, "factor": factor,
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -438,6 +464,13 @@ def run_ours(args, w):
     barrier(world)
     ms_local = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms_local, world)
+    # host cost of one call (argument checks, cached tensor descriptors, launch), enqueue only
+    n_h = max(3, args.steps)
+    t_h = time.perf_counter()
+    for _ in range(n_h):
+        call(head_factor)
+    host_us = (time.perf_counter() - t_h) * 1e6 / n_h
+    torch.cuda.synchronize()
     value = job_throughput(dense, world, ms) / 1e12
     achieved = ex / (ms_local * 1e-3) / 1e12
 
@@ -468,10 +501,40 @@ def run_ours(args, w):
         stream.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
         e2e_ms = max_over_ranks(e2e_ms, world)
+        h2d_bytes = int(3 * q.nbytes)
+        d2h_bytes = int(oh.numel() * 2 + lh.numel() * 4)
+        # Diagnosis (outside the timed steps): each step again on its own, followed by plain
+        # contiguous copies of the same bytes in each direction, so that a step that ran slow can
+        # be told apart as host-link bound (the probe copies slow too) or not.
+        step_ms, h2d_gbs, d2h_gbs = [], [], []
+        probe_in = torch.empty(h2d_bytes, dtype=torch.uint8, device="cuda")
+        probe_src = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+        probe_out = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for _ in range(n_e2e):
+            t1 = time.perf_counter()
+            e2e_step()
+            stream.synchronize()
+            step_ms.append((time.perf_counter() - t1) * 1e3)
+            with torch.cuda.stream(stream):
+                ev[0].record(stream)
+                probe_in.copy_(probe_src, non_blocking=True)
+                ev[1].record(stream)
+                probe_out.copy_(probe_in[:d2h_bytes], non_blocking=True)
+                ev[2].record(stream)
+            ev[2].synchronize()
+            h2d_gbs.append(h2d_bytes / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
+            d2h_gbs.append(d2h_bytes / (ev[1].elapsed_time(ev[2]) * 1e-3) / 1e9)
+        del probe_in, probe_src, probe_out
         e2e = {"value": job_throughput(dense, world, e2e_ms) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                "steps": n_e2e, "api": "blasst_attn_fwd_host", "heads_per_group": hpg,
-               "h2d_bytes_per_step": int(3 * q.nbytes),
-               "d2h_bytes_per_step": int(oh.numel() * 2 + lh.numel() * 4)}
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "diagnosis": {"step_ms": [round(x, 3) for x in step_ms],
+                             "h2d_probe_gbs": [round(x, 1) for x in h2d_gbs],
+                             "d2h_probe_gbs": [round(x, 1) for x in d2h_gbs],
+                             "kernel_ms": ms_local,
+                             "note": "each step re-run alone, then one contiguous pinned copy of the step's "
+                                     "input bytes H2D and output bytes D2H (CUDA events)"}}
         del ws
 
     cpu = None
@@ -479,16 +542,28 @@ def run_ours(args, w):
         import oracle
         oracle.build()
         threads = min(os.cpu_count() or 1, args.cpu_units)
+        n_all = w.B * w.H * nQ
         rate, dt, units = cpu_oracle_rate(w, q, k, v, head_factor, args.cpu_units, threads)
         # the same oracle on one core, on a smaller sample (query tiles are independent, so the
         # rate does not depend on the sample's size)
         n1 = max(1, min(4, args.cpu_units))
         rate1, dt1, units1 = cpu_oracle_rate(w, q, k, v, head_factor, n1, 1)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+        # and on one core over a whole call of the smallest workload (every query tile)
+        wt = synth.WORKLOADS["tiny_1024"]
+        qt_, kt_, vt_ = synth.make_qkv(wt)
+        ft = max(workload_factors(wt))
+        rate_t, dt_t, units_t = cpu_oracle_rate(wt, qt_, kt_, vt_, ft, 0, 1, units="all")
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"{len(units)} query tiles (batch 0, heads 0 and {w.H - 1}, first tiles) of "
-                         f"{w.name} at factor {head_factor:g}; {dt:.1f} s wall",
+                         f"{w.name} at factor {head_factor:g}, {threads} threads; {dt:.1f} s wall; rate "
+                         f"extrapolated to the whole call from {len(units)} of {n_all} query tiles",
                "single_core": {"value": rate1, "unit": UNIT, "cores": 1,
-                               "sample": f"{len(units1)} query tiles of the same sample; {dt1:.1f} s wall"}}
+                               "sample": f"{len(units1)} query tiles of the same sample; {dt1:.1f} s wall; "
+                                         f"extrapolated from {len(units1)} of {n_all} query tiles"},
+               "single_core_full_call": {"value": rate_t, "unit": UNIT, "cores": 1, "workload": wt.name,
+                                         "factor": ft, "s": dt_t,
+                                         "sample": f"the whole {wt.name} call ({len(units_t)} query tiles), "
+                                                   f"not extrapolated"}}
 
     if rank == 0:
         line = {
@@ -507,6 +582,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
+            "host_enqueue_us_per_call": host_us,
             "clocks": clocks.summary(),
             "sweep": sweep,
             "extras": extras,
