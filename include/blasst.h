@@ -43,7 +43,8 @@ typedef enum blasst_status {
   BLASST_ERR_INVALID_ARG = 1,        /* an argument is outside the documented domain */
   BLASST_ERR_UNSUPPORTED_DEVICE = 2, /* the current device is not compute capability 10.3 */
   BLASST_ERR_LAUNCH = 3,             /* the CUDA runtime refused a launch, copy or set-up step */
-  BLASST_ERR_TIMEOUT = 4             /* a device-side wait gave up (see blasst_device_error) */
+  BLASST_ERR_TIMEOUT = 4,            /* a device-side wait gave up (see blasst_device_error) */
+  BLASST_ERR_TOO_LARGE = 5           /* the problem does not fit a fixed-size library buffer */
 } blasst_status;
 
 /*
@@ -187,6 +188,43 @@ typedef struct blasst_host_args {
 size_t blasst_host_workspace_bytes(int B, int H, int Sq, int Sk, int heads_per_group);
 
 blasst_status blasst_attn_fwd_host(const blasst_host_args *args);
+
+/*
+ * Host-buffer call that allocates nothing. It has no counterpart in the method or on the pages
+ * that describe it: it exists for callers that cannot call cudaMalloc. Examples are a plug-in
+ * loaded into a host application that keeps all of the GPU's memory in its own pool and hands
+ * out no raw device buffers, and a latency-critical loop that must not call cudaMalloc or
+ * cudaFree, which can synchronize the whole device.
+ *
+ * The call is blasst_attn_fwd_host with its device workspace taken from a buffer of
+ * BLASST_NOALLOC_SCRATCH_BYTES bytes that the library itself holds: a fixed-size __device__
+ * array. The CUDA runtime reserves it on a device when it loads the library's code there and
+ * releases it only when the process exits. With lazy module loading (the CUDA default) that
+ * happens at this entry point's first call on the device; with eager loading, when the context
+ * is created.
+ *
+ *   args   as for blasst_attn_fwd_host, except that workspace must be NULL and workspace_bytes
+ *          0. heads_per_group (1 .. H) is the largest head group wanted: the call lowers it to
+ *          the largest group whose two workspace slots fit the buffer.
+ *
+ * The call returns BLASST_ERR_TOO_LARGE, with nothing enqueued, when even a group of one head
+ * does not fit, that is when blasst_host_workspace_bytes(B, H, Sq, Sk, 1) exceeds
+ * BLASST_NOALLOC_SCRATCH_BYTES. Otherwise it returns what blasst_attn_fwd_host returns. It
+ * never calls cudaMalloc, cudaFree or any library routine that allocates device memory.
+ *
+ * Set-up: the first call on a device, made with that device current, looks up the buffer's
+ * device address there (cudaGetSymbolAddress). That lookup loads the library's code on the
+ * device if it is not loaded yet. Make that first call before any stream capture begins.
+ *
+ * Sharing: every call on a device uses the same buffer, and the buffer keeps the last call's
+ * contents. Each call writes every byte of the buffer it reads before reading it (its copies of
+ * q, k and v; the kernel writes all of o and lse), so nothing needs clearing between calls.
+ * Calls whose GPU work overlaps race on the buffer. A call starts after earlier work on its
+ * `stream`, so calls on one stream are safe. Calls on different streams, or from different
+ * threads, must be ordered by the caller.
+ */
+#define BLASST_NOALLOC_SCRATCH_BYTES ((size_t)256 << 20)
+blasst_status blasst_attn_fwd_host_noalloc(const blasst_host_args *args);
 
 /* A static, human-readable name for a status code. */
 const char *blasst_status_string(blasst_status s);

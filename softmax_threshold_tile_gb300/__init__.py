@@ -9,7 +9,9 @@ from ._binding import (  # noqa: F401
     BLASST_ERR_INVALID_ARG,
     BLASST_ERR_LAUNCH,
     BLASST_ERR_TIMEOUT,
+    BLASST_ERR_TOO_LARGE,
     BLASST_ERR_UNSUPPORTED_DEVICE,
+    BLASST_NOALLOC_SCRATCH_BYTES,
     BLASST_OK,
     BLASST_QK_BF16,
     BLASST_QK_E4M3,
@@ -23,6 +25,7 @@ from ._binding import (  # noqa: F401
     attn_fwd_host,
     host_workspace,
     blasst_attn_fwd_host,
+    blasst_attn_fwd_host_noalloc,
     blasst_debug_withhold_key_tile,
     blasst_host_workspace_bytes,
     blasst_tensor_map_encodes,

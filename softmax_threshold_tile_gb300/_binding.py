@@ -18,6 +18,10 @@ BLASST_ERR_INVALID_ARG = 1
 BLASST_ERR_UNSUPPORTED_DEVICE = 2
 BLASST_ERR_LAUNCH = 3
 BLASST_ERR_TIMEOUT = 4
+BLASST_ERR_TOO_LARGE = 5
+
+# Size of the library's own device buffer used by blasst_attn_fwd_host_noalloc.
+BLASST_NOALLOC_SCRATCH_BYTES = 256 << 20
 
 BLASST_QK_BF16 = 0
 BLASST_QK_E4M3 = 1
@@ -102,6 +106,8 @@ def load_library(path: str | None = None):
     lib.blasst_debug_withhold_key_tile.argtypes = [ctypes.c_int]
     lib.blasst_tensor_map_encodes.restype = ctypes.c_uint64
     lib.blasst_tensor_map_encodes.argtypes = []
+    lib.blasst_attn_fwd_host_noalloc.restype = ctypes.c_int
+    lib.blasst_attn_fwd_host_noalloc.argtypes = [ctypes.POINTER(HostArgs)]
     dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
     lib.blasst_factor_from_threshold.restype = ctypes.c_int
     lib.blasst_factor_from_threshold.argtypes = [ctypes.c_double, ctypes.c_int64, dp]
@@ -173,6 +179,21 @@ def blasst_attn_fwd_host(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, worksp
     return int(load_library().blasst_attn_fwd_host(ctypes.byref(a)))
 
 
+def blasst_attn_fwd_host_noalloc(q, k, v, o, lse, B, H, Sq, Sk, d, scale, factor, heads_per_group,
+                                 stream) -> int:
+    """The host-buffer C entry point that allocates nothing (its workspace is the library's own
+    fixed device buffer); q / k / v / o / lse are HOST addresses (or CPU tensors)."""
+    a = HostArgs()
+    a.struct_size = ctypes.sizeof(HostArgs)
+    a.q, a.k, a.v, a.o, a.lse = _p(q), _p(k), _p(v), _p(o), _p(lse)
+    a.B, a.H, a.Sq, a.Sk, a.d = int(B), int(H), int(Sq), int(Sk), int(d)
+    a.scale, a.factor = float(scale), float(factor)
+    a.workspace, a.workspace_bytes = None, 0
+    a.heads_per_group = int(heads_per_group)
+    a.stream = _p(stream)
+    return int(load_library().blasst_attn_fwd_host_noalloc(ctypes.byref(a)))
+
+
 def blasst_debug_withhold_key_tile(tile: int) -> int:
     """Test hook of the bounded device waits: the producer withholds the copy of key tile `tile`
     in every launch from now on (-1: off)."""
@@ -189,7 +210,8 @@ def blasst_status_string(code: int) -> str:
         return load_library().blasst_status_string(int(code)).decode()
     except RuntimeError:
         return {0: "ok", 1: "invalid argument", 2: "unsupported device", 3: "CUDA launch or set-up failure",
-                4: "a device-side wait timed out"}.get(int(code), "unknown status")
+                4: "a device-side wait timed out", 5: "too large for the library's fixed buffer"}.get(
+                    int(code), "unknown status")
 
 
 def blasst_device_error(clear: bool = True) -> tuple[int, int]:

@@ -11,8 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libblasst_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["blasst_fwd.cu", "blasst_host.cpp"]
-HEADERS = ["sm103_ptx.cuh"]
+SOURCES = ["blasst_fwd.cu", "blasst_noalloc.cu", "blasst_host.cpp"]
+HEADERS = ["sm103_ptx.cuh", "blasst_internal.h"]
 INCLUDE = os.path.join(ROOT, "include")
 
 NVCC_FLAGS = [

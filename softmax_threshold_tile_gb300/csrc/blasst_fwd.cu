@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "blasst.h"
+#include "blasst_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace blasst {
@@ -1151,6 +1152,10 @@ blasst_status launch_host(const blasst_host_args& a) {
 
 }  // namespace
 
+blasst_status run_host_pipeline(const blasst_host_args& a) { return launch_host(a); }
+
+blasst_status check_device() { return prepare_device(); }
+
 }  // namespace blasst
 
 extern "C" size_t blasst_host_workspace_bytes(int B, int H, int Sq, int Sk, int heads_per_group) {
@@ -1207,6 +1212,7 @@ extern "C" const char* blasst_status_string(blasst_status s) {
     case BLASST_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
     case BLASST_ERR_LAUNCH: return "CUDA launch or set-up failure";
     case BLASST_ERR_TIMEOUT: return "a device-side wait timed out or packed-document offsets were invalid";
+    case BLASST_ERR_TOO_LARGE: return "the problem does not fit the library's fixed-size buffer";
   }
   return "unknown status";
 }

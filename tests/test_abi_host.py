@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         assert blasst.blasst_status_string(code)
     assert blasst.blasst_version() >= 100
 
