@@ -42,6 +42,7 @@ METRIC = "ms/call and dense-equiv TFLOPS vs skip fraction, bf16 d=128, S=32760, 
 KERNEL_SOURCES = ["softmax_threshold_tile_gb300/csrc/blasst_fwd.cu", "softmax_threshold_tile_gb300/csrc/sm103_ptx.cuh"]
 NCU_TRAFFIC = {
     "265a36ec00c0eed3": {"workload": "wan_32760", "factor": 32.0, "bytes": 1008250112 + 322755328},
+    "f126bb95c3f763e9": {"workload": "wan_32760", "factor": 32.0, "bytes": 1007854848 + 322692096},
 }
 UNIT = "TFLOPS (dense-equivalent)"
 TILE = 128

@@ -98,7 +98,9 @@ struct alignas(1024) Smem {
   uint64_t q_full;
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
-  uint64_t s_full[kQTiles];   // S of tile t is ready in TMEM (tcgen05.commit)
+  // S of tile t for key tile j is ready in TMEM (tcgen05.commit): slot j % 2 in the lambda = 0
+  // instance, whose producer waits on it too; slot 0 (phase j) otherwise.
+  uint64_t s_full[kQTiles][2];
   uint64_t dec[kQTiles][2];   // tile t has decided key tile j (slot j % 2); flag in skip_flag
   uint64_t p_ready[kQTiles];  // softmax t is done with S: decision taken, P written, O rescaled
   uint64_t o_done[kQTiles];   // every MMA of the CTA has completed (one phase, after the loop)
@@ -108,8 +110,7 @@ struct alignas(1024) Smem {
   uint32_t quit[kQTiles][2];  // the softmax warps leave the loop together (tile, step parity)
   float hmax[kQTiles][2][kTile];   // half-row maxima of the current key tile (tile, half, row)
   float lpart[kQTiles][2][kTile];  // half-row sums at the end (tile, half, row)
-  uint32_t abort;             // some role gave up waiting
-  uint32_t* status;           // the caller's device status word, or null
+  uint32_t abort;             // non-zero once some role gave up waiting: the roles' error bits
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the base to 1024 B
 
@@ -209,20 +210,20 @@ __device__ __forceinline__ Geo make_geo(const FwdParams& p, int b, int h) {
 }
 
 // Bounded wait on an mbarrier phase. Gives up after `timeout_ns`, or at once when
-// another role has given up (unless `respect_abort` is false); on a timeout it
-// records `site` in the device error word and raises the CTA abort flag.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem& sm, uint32_t site,
-                                         bool respect_abort = true, uint64_t timeout_ns = kWaitTimeoutNs) {
+// another role has given up (unless `respect_abort` is false); on a timeout it ORs `site` into
+// the CTA's abort word, which the CTA reports device-wide (and to the caller's status word) when
+// it ends.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                         uint32_t site, bool respect_abort = true,
+                                         uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  volatile uint32_t* abort = &sm.abort;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (respect_abort && *abort) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
-        *abort = 1u;
-        report_error(sm.status, site);
+        atomicOr(const_cast<uint32_t*>(abort), site);  // reported when the CTA ends
         return false;
       }
     }
@@ -242,6 +243,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
                                              const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
                                              int qt0) {
   const Lens<kVarlen> L{p, g};
+  volatile uint32_t* abort = &sm.abort;
   prefetch_tmap(tq);
   prefetch_tmap(tk);
   prefetch_tmap(tv);
@@ -292,13 +294,15 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     // lambda = 0: every key tile is kept, so no decision is waited for. K_(j+1) and V_j go out
     // together, and the stages are released by the scores instead: S_B(j) is committed after
     // every MMA up to Q_B K_j^T, which covers the readers of K_j and of V_(j-1), the tiles the
-    // next iteration's copies overwrite. The softmax warps report that they saw S_B(j) on
-    // dec[B][j % 2]: each slot is waited once per use, and its next phase (key tile j + 2)
-    // needs K_(j+2), which is issued only after this wait, so the parity cannot alias.
+    // next iteration's copies overwrite. In this instance the scores of key tile j are committed
+    // to slot j % 2: each slot is waited once per use, and its next phase (key tile j + 2) needs
+    // K_(j+2), which is issued only after this wait, so the parity cannot alias. (Alternating the
+    // slots costs ~1 % of the time, so the general instance, whose producer never waits on the
+    // scores, keeps one slot.)
     for (int j = 0; j < L.nK() && ok; ++j) {
       if (j + 1 < L.nK()) issue_k(j + 1);
       issue_v(j);
-      ok = wait_bar(smem_u32(&sm.dec[kQTiles - 1][j & 1]), (j >> 1) & 1, sm, kErrProducer);
+      ok = wait_bar(smem_u32(&sm.s_full[kQTiles - 1][j & 1]), (j >> 1) & 1, abort, kErrProducer);
     }
   }
   for (int j = 0; j < L.nK() && ok && !kDense; ++j) {
@@ -309,7 +313,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
     bool loaded = false;
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {
-      if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, sm, kErrProducer)) { ok = false; break; }
+      if (!wait_bar(smem_u32(&sm.dec[t][j & 1]), (j >> 1) & 1, abort, kErrProducer)) { ok = false; break; }
       const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
       if (!skip && !loaded) {
         issue_v(j);
@@ -322,17 +326,18 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   for (int back = 1; back <= kStages; ++back) {
     const int nk = k_issued - back, nv = v_issued - back;
     if (nk >= 0)
-      wait_bar(smem_u32(&sm.k_full[nk & 1]), (nk >> 1) & 1, sm, kErrDrain, false, kDrainTimeoutNs);
+      wait_bar(smem_u32(&sm.k_full[nk & 1]), (nk >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
     if (nv >= 0)
-      wait_bar(smem_u32(&sm.v_full[nv & 1]), (nv >> 1) & 1, sm, kErrDrain, false, kDrainTimeoutNs);
+      wait_bar(smem_u32(&sm.v_full[nv & 1]), (nv >> 1) & 1, abort, kErrDrain, false, kDrainTimeoutNs);
   }
-  wait_bar(q_full, 0, sm, kErrDrain, false, kDrainTimeoutNs);
+  wait_bar(q_full, 0, abort, kErrDrain, false, kDrainTimeoutNs);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 template <bool kVarlen, bool kFp8, bool kDense>
 __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
   const Lens<kVarlen> L{p, g};
+  volatile uint32_t* abort = &sm.abort;
   constexpr uint32_t kIdescQK = kFp8 ? idesc_e4m3_f32(kTile, kTile)          // K tile is K-major
                                      : idesc_bf16_f32(kTile, kTile, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kTile, kHeadDim, true);   // V tile is MN-major
@@ -387,14 +392,14 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   };
 
   int pv_issued0 = 0, pv_issued1 = 0;
-  bool ok = wait_bar(smem_u32(&sm.q_full), 0, sm, kErrMma) &&
-            wait_bar(smem_u32(&sm.k_full[0]), 0, sm, kErrMma);
+  bool ok = wait_bar(smem_u32(&sm.q_full), 0, abort, kErrMma) &&
+            wait_bar(smem_u32(&sm.k_full[0]), 0, abort, kErrMma);
   if (ok) {
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {
       issue_qk(t, 0);
-      tc_commit(smem_u32(&sm.s_full[t]));
+      tc_commit(smem_u32(&sm.s_full[t][0]));  // key tile 0: slot 0 in either scheme
     }
     int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
     for (int j = 0; j < L.nK() && ok; ++j) {
@@ -408,13 +413,13 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
       for (int t = 0; t < kQTiles; ++t) {
         // p_ready arrives once the tile has read S_t and decided: at once for a skipped
         // key tile, after P is written (and O rescaled) for a kept one.
-        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, sm, kErrMma)) { ok = false; break; }
+        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
         tc_fence_after();
         // (lambda = 0 keeps every key tile: no decision to read.)
         const uint32_t skip = kDense ? 0u : *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
         if (!skip) {
           if (!v_ready) {
-            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, sm, kErrMma)) { ok = false; break; }
+            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
             tc_fence_after();
             v_ready = true;
           }
@@ -426,11 +431,11 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
           // S_t is free: it was read before p_ready, and its P (if the tile was kept) is
           // read by the P V just issued; tcgen05.mma executes in issue order.
           if (t == 0) {
-            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, sm, kErrMma)) { ok = false; break; }
+            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, abort, kErrMma)) { ok = false; break; }
             tc_fence_after();
           }
           issue_qk(t, nst);
-          tc_commit(smem_u32(&sm.s_full[t]));
+          tc_commit(smem_u32(&sm.s_full[t][kDense ? nst : 0]));
         }
       }
       if (!ok) break;
@@ -445,7 +450,7 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   for (int t = 0; t < kQTiles; ++t) tc_commit(smem_u32(&sm.o_done[t]));
   // Every MMA this thread issued completes before TMEM is released.
   tc_commit(smem_u32(&sm.drain));
-  wait_bar(smem_u32(&sm.drain), 0, sm, kErrDrain, false, kDrainTimeoutNs);
+  wait_bar(smem_u32(&sm.drain), 0, abort, kErrDrain, false, kDrainTimeoutNs);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -472,6 +477,7 @@ template <bool kVarlen, bool kMaxProb, bool kDense>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
                                             int b, int h, int qt0) {
   const Lens<kVarlen> L{p, g};
+  volatile uint32_t* abort = &sm.abort;
   const int warp = threadIdx.x >> 5;
   const int wq = warp & 3;                // TMEM lane quarter
   const int half = warp >> 2;             // key columns 64 * half ... + 63; O features likewise
@@ -494,10 +500,9 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     float hmax = -INFINITY;
     uint32_t sr[64];
     if (!failed) {
-      const bool ok = wait_bar(smem_u32(&sm.s_full[t]), j & 1, sm, kErrSoftmax);
+      const bool ok = kDense ? wait_bar(smem_u32(&sm.s_full[t][j & 1]), (j >> 1) & 1, abort, kErrSoftmax)
+                             : wait_bar(smem_u32(&sm.s_full[t][0]), j & 1, abort, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
-      // lambda = 0: tell the producer that S_B(j) has completed (it reuses the stages then).
-      if (kDense && t == kQTiles - 1 && leader && !failed) mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
     }
     if (!failed) {
       tc_fence_after();
@@ -616,8 +621,8 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   sm.lpart[0][half][row] = cur.l;
   sm.lpart[1][half][row] = oth.l;
   bar_sync_n<2 * kSoftmaxThreads>(3u);
-  const bool ok = failed ? false : wait_bar(smem_u32(&sm.o_done[0]), 0, sm, kErrSoftmax) &&
-                                       wait_bar(smem_u32(&sm.o_done[1]), 0, sm, kErrSoftmax);
+  const bool ok = failed ? false : wait_bar(smem_u32(&sm.o_done[0]), 0, abort, kErrSoftmax) &&
+                                       wait_bar(smem_u32(&sm.o_done[1]), 0, abort, kErrSoftmax);
   if (!__all_sync(0xffffffffu, ok)) return;
   tc_fence_after();
 #pragma unroll 1
@@ -698,7 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.v_full[s]), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
-      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.s_full[t][0]), 1);
+      mbar_init(smem_u32(&sm.s_full[t][1]), 1);
       mbar_init(smem_u32(&sm.dec[t][0]), 1);
       mbar_init(smem_u32(&sm.dec[t][1]), 1);
       mbar_init(smem_u32(&sm.p_ready[t]), kQTiles * kSoftmaxWarps);
@@ -710,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0u;
-    sm.status = p.status;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -740,6 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A wait that gave up left its role's bit in the abort word: report it device-wide and to the
+  // caller's status word.
+  if (threadIdx.x == 0) {
+    const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&sm.abort);
+    if (bits) report_error(p.status, bits);
+  }
   if ((threadIdx.x >> 5) == kMmaWarp) {
     Smem& sm2 = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
