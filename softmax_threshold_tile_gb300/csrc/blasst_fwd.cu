@@ -17,15 +17,14 @@
 //              barrier, which also publishes the half-row maxima), exp2 of a kept
 //              tile written back into TMEM as bf16 P (over S_j), conditional O
 //              rescale, epilogue (O / l -> bf16, lse).
-//   warp 8     MMA: one thread issues tcgen05.mma, alternating the two tiles so
-//              that one tile's softmax overlaps the other tile's matrix work:
+//   warp 8     MMA: the whole warp runs the issue loop and one elected lane issues
+//              tcgen05.mma, alternating the two tiles so that one tile's softmax
+//              overlaps the other tile's matrix work:
 //                O_A += P_A(j) V_j ; S_A = Q_A K_{j+1}^T ; O_B += P_B(j) V_j ; S_B = Q_B K_{j+1}^T
 //              P V is issued only for a tile that kept key tile j.
 //   warp 9     TMA producer: both Q tiles once, K tiles one ahead through a 2-stage ring,
 //              and V_j only once a tile has kept key tile j (as soon as tile A keeps it,
 //              otherwise after tile B's decision): a key tile both tiles skip is never loaded.
-// With lambda = 0 (and bf16 scores) nothing can be skipped: a separate instance publishes
-// and reads no decisions, and copies every V_j together with K_(j+1).
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Shared memory: Q_A, Q_B, 2 x K, 2 x V tiles of 32 KiB, all 128-byte swizzled.
 //
@@ -98,9 +97,7 @@ struct alignas(1024) Smem {
   uint64_t q_full;
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
-  // S of tile t for key tile j is ready in TMEM (tcgen05.commit): slot j % 2 in the lambda = 0
-  // instance, whose producer waits on it too; slot 0 (phase j) otherwise.
-  uint64_t s_full[kQTiles][2];
+  uint64_t s_full[kQTiles];   // S of tile t for key tile j is in TMEM (tcgen05.commit, phase j)
   uint64_t dec[kQTiles][2];   // tile t has decided key tile j (slot j % 2); flag in skip_flag
   uint64_t p_ready[kQTiles];  // softmax t is done with S: decision taken, P written, O rescaled
   uint64_t o_done[kQTiles];   // every MMA of the CTA has completed (one phase, after the loop)
@@ -238,7 +235,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ producer
-template <bool kVarlen, bool kFp8, bool kDense>
+template <bool kVarlen, bool kFp8>
 __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
                                              const CUtensorMap* tv, const FwdParams& p, const Geo& g, int h,
                                              int qt0) {
@@ -290,22 +287,7 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
   };
   issue_k(0);
   bool ok = true;
-  if (kDense) {
-    // lambda = 0: every key tile is kept, so no decision is waited for. K_(j+1) and V_j go out
-    // together, and the stages are released by the scores instead: S_B(j) is committed after
-    // every MMA up to Q_B K_j^T, which covers the readers of K_j and of V_(j-1), the tiles the
-    // next iteration's copies overwrite. In this instance the scores of key tile j are committed
-    // to slot j % 2: each slot is waited once per use, and its next phase (key tile j + 2) needs
-    // K_(j+2), which is issued only after this wait, so the parity cannot alias. (Alternating the
-    // slots costs ~1 % of the time, so the general instance, whose producer never waits on the
-    // scores, keeps one slot.)
-    for (int j = 0; j < L.nK() && ok; ++j) {
-      if (j + 1 < L.nK()) issue_k(j + 1);
-      issue_v(j);
-      ok = wait_bar(smem_u32(&sm.s_full[kQTiles - 1][j & 1]), (j >> 1) & 1, abort, kErrProducer);
-    }
-  }
-  for (int j = 0; j < L.nK() && ok && !kDense; ++j) {
+  for (int j = 0; j < L.nK() && ok; ++j) {
     if (j + 1 < L.nK()) issue_k(j + 1);
     // V_j is needed if either tile keeps key tile j. Both decisions are waited for on every
     // j, so each decision barrier slot is waited once per use and its parity cannot alias (a
@@ -334,7 +316,16 @@ __device__ __forceinline__ void run_producer(Smem& sm, const CUtensorMap* tq, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <bool kVarlen, bool kFp8, bool kDense>
+// Every lane of a converged warp waits; the result is the same in every lane.
+__device__ __forceinline__ bool wait_bar_w(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                           uint32_t site, bool respect_abort = true,
+                                           uint64_t timeout_ns = kWaitTimeoutNs) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, site, respect_abort, timeout_ns));
+}
+
+// Run by all 32 lanes of the MMA warp. Waits and flag reads give every lane the same result, so
+// the warp stays converged, and one elected lane (always lane 0) issues the MMAs and commits.
+template <bool kVarlen, bool kFp8>
 __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g) {
   const Lens<kVarlen> L{p, g};
   volatile uint32_t* abort = &sm.abort;
@@ -359,20 +350,20 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
     const uint32_t d = tmem + col_s(t);
     if (kFp8) {
       // e4m3: 4 steps of K = 32 features, 32 B apart inside the one 128-B swizzled row.
-      mma_ss_f8_off<0, 0>(d, aq, bk, kIdescQK, 0u);
-      mma_ss_f8_off<2, 2>(d, aq, bk, kIdescQK, 1u);
-      mma_ss_f8_off<4, 4>(d, aq, bk, kIdescQK, 1u);
-      mma_ss_f8_off<6, 6>(d, aq, bk, kIdescQK, 1u);
+      mma_ss_f8_off_w<0, 0>(d, aq, bk, kIdescQK, 0u);
+      mma_ss_f8_off_w<2, 2>(d, aq, bk, kIdescQK, 1u);
+      mma_ss_f8_off_w<4, 4>(d, aq, bk, kIdescQK, 1u);
+      mma_ss_f8_off_w<6, 6>(d, aq, bk, kIdescQK, 1u);
       return;
     }
-    mma_ss_off<0, 0>(d, aq, bk, kIdescQK, 0u);
-    mma_ss_off<2, 2>(d, aq, bk, kIdescQK, 1u);       // +32 B
-    mma_ss_off<4, 4>(d, aq, bk, kIdescQK, 1u);       // +64 B
-    mma_ss_off<6, 6>(d, aq, bk, kIdescQK, 1u);       // +96 B
-    mma_ss_off<1024, 1024>(d, aq, bk, kIdescQK, 1u); // second 64-feature half (+16 KiB)
-    mma_ss_off<1026, 1026>(d, aq, bk, kIdescQK, 1u);
-    mma_ss_off<1028, 1028>(d, aq, bk, kIdescQK, 1u);
-    mma_ss_off<1030, 1030>(d, aq, bk, kIdescQK, 1u);
+    mma_ss_off_w<0, 0>(d, aq, bk, kIdescQK, 0u);
+    mma_ss_off_w<2, 2>(d, aq, bk, kIdescQK, 1u);       // +32 B
+    mma_ss_off_w<4, 4>(d, aq, bk, kIdescQK, 1u);       // +64 B
+    mma_ss_off_w<6, 6>(d, aq, bk, kIdescQK, 1u);       // +96 B
+    mma_ss_off_w<1024, 1024>(d, aq, bk, kIdescQK, 1u); // second 64-feature half (+16 KiB)
+    mma_ss_off_w<1026, 1026>(d, aq, bk, kIdescQK, 1u);
+    mma_ss_off_w<1028, 1028>(d, aq, bk, kIdescQK, 1u);
+    mma_ss_off_w<1030, 1030>(d, aq, bk, kIdescQK, 1u);
   };
   // O_t (+)= P_t V: 8 steps of K = 16 keys. P sits in TMEM over S_t (2 bf16 per column, 8
   // columns per step). V rows are keys: a step advances 16 rows = 2 KiB (128 in the
@@ -381,25 +372,25 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
     const uint64_t bv = st ? dv1 : dv0;
     const uint32_t d = tmem + col_o(t);
     const uint32_t a = tmem + col_s(t);
-    mma_ts_off<0>(d, a, bv, kIdescPV, accumulate ? 1u : 0u);
-    mma_ts_off<128>(d, a + 8, bv, kIdescPV, 1u);
-    mma_ts_off<256>(d, a + 16, bv, kIdescPV, 1u);
-    mma_ts_off<384>(d, a + 24, bv, kIdescPV, 1u);
-    mma_ts_off<512>(d, a + 32, bv, kIdescPV, 1u);
-    mma_ts_off<640>(d, a + 40, bv, kIdescPV, 1u);
-    mma_ts_off<768>(d, a + 48, bv, kIdescPV, 1u);
-    mma_ts_off<896>(d, a + 56, bv, kIdescPV, 1u);
+    mma_ts_off_w<0>(d, a, bv, kIdescPV, accumulate ? 1u : 0u);
+    mma_ts_off_w<128>(d, a + 8, bv, kIdescPV, 1u);
+    mma_ts_off_w<256>(d, a + 16, bv, kIdescPV, 1u);
+    mma_ts_off_w<384>(d, a + 24, bv, kIdescPV, 1u);
+    mma_ts_off_w<512>(d, a + 32, bv, kIdescPV, 1u);
+    mma_ts_off_w<640>(d, a + 40, bv, kIdescPV, 1u);
+    mma_ts_off_w<768>(d, a + 48, bv, kIdescPV, 1u);
+    mma_ts_off_w<896>(d, a + 56, bv, kIdescPV, 1u);
   };
 
   int pv_issued0 = 0, pv_issued1 = 0;
-  bool ok = wait_bar(smem_u32(&sm.q_full), 0, abort, kErrMma) &&
-            wait_bar(smem_u32(&sm.k_full[0]), 0, abort, kErrMma);
+  bool ok = wait_bar_w(smem_u32(&sm.q_full), 0, abort, kErrMma) &&
+            wait_bar_w(smem_u32(&sm.k_full[0]), 0, abort, kErrMma);
   if (ok) {
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {
       issue_qk(t, 0);
-      tc_commit(smem_u32(&sm.s_full[t][0]));  // key tile 0: slot 0 in either scheme
+      tc_commit_w(smem_u32(&sm.s_full[t]));
     }
     int v_used = 0;  // V tiles consumed so far; V copy n sits in stage n % 2
     for (int j = 0; j < L.nK() && ok; ++j) {
@@ -413,13 +404,12 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
       for (int t = 0; t < kQTiles; ++t) {
         // p_ready arrives once the tile has read S_t and decided: at once for a skipped
         // key tile, after P is written (and O rescaled) for a kept one.
-        if (!wait_bar(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
+        if (!wait_bar_w(smem_u32(&sm.p_ready[t]), j & 1, abort, kErrMma)) { ok = false; break; }
         tc_fence_after();
-        // (lambda = 0 keeps every key tile: no decision to read.)
-        const uint32_t skip = kDense ? 0u : *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
+        const uint32_t skip = *reinterpret_cast<volatile uint32_t*>(&sm.skip_flag[t][j & 1]);
         if (!skip) {
           if (!v_ready) {
-            if (!wait_bar(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
+            if (!wait_bar_w(smem_u32(&sm.v_full[st]), parity, abort, kErrMma)) { ok = false; break; }
             tc_fence_after();
             v_ready = true;
           }
@@ -431,11 +421,11 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
           // S_t is free: it was read before p_ready, and its P (if the tile was kept) is
           // read by the P V just issued; tcgen05.mma executes in issue order.
           if (t == 0) {
-            if (!wait_bar(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, abort, kErrMma)) { ok = false; break; }
+            if (!wait_bar_w(smem_u32(&sm.k_full[nst]), ((j + 1) >> 1) & 1, abort, kErrMma)) { ok = false; break; }
             tc_fence_after();
           }
           issue_qk(t, nst);
-          tc_commit(smem_u32(&sm.s_full[t][kDense ? nst : 0]));
+          tc_commit_w(smem_u32(&sm.s_full[t]));
         }
       }
       if (!ok) break;
@@ -447,10 +437,10 @@ __device__ __forceinline__ void run_mma(Smem& sm, uint32_t tmem, const FwdParams
   // earlier MMA of this thread, so a softmax that has S_t(j + 1) knows its earlier P V are
   // done. Committed on every exit path, so the epilogue waits never hang.
 #pragma unroll
-  for (int t = 0; t < kQTiles; ++t) tc_commit(smem_u32(&sm.o_done[t]));
+  for (int t = 0; t < kQTiles; ++t) tc_commit_w(smem_u32(&sm.o_done[t]));
   // Every MMA this thread issued completes before TMEM is released.
-  tc_commit(smem_u32(&sm.drain));
-  wait_bar(smem_u32(&sm.drain), 0, abort, kErrDrain, false, kDrainTimeoutNs);
+  tc_commit_w(smem_u32(&sm.drain));
+  wait_bar_w(smem_u32(&sm.drain), 0, abort, kErrDrain, false, kDrainTimeoutNs);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -473,7 +463,7 @@ __device__ __forceinline__ void swap_state(TileState& a, TileState& b) {
   b = tmp;
 }
 
-template <bool kVarlen, bool kMaxProb, bool kDense>
+template <bool kVarlen, bool kMaxProb>
 __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdParams& p, const Geo& g,
                                             int b, int h, int qt0) {
   const Lens<kVarlen> L{p, g};
@@ -500,8 +490,7 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     float hmax = -INFINITY;
     uint32_t sr[64];
     if (!failed) {
-      const bool ok = kDense ? wait_bar(smem_u32(&sm.s_full[t][j & 1]), (j >> 1) & 1, abort, kErrSoftmax)
-                             : wait_bar(smem_u32(&sm.s_full[t][0]), j & 1, abort, kErrSoftmax);
+      const bool ok = wait_bar(smem_u32(&sm.s_full[t]), j & 1, abort, kErrSoftmax);
       failed = !__all_sync(0xffffffffu, ok);
     }
     if (!failed) {
@@ -537,12 +526,9 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
     do {
       if (leader) {
         // Publish the decision: the producer loads V_j only if some tile keeps key tile j,
-        // and the MMA issues P V only for a kept tile. (With lambda = 0 both act on every
-        // key tile without it.)
-        if (!kDense) {
-          sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
-          mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
-        }
+        // and the MMA issues P V only for a kept tile.
+        sm.skip_flag[t][j & 1] = skip ? 1u : 0u;
+        mbar_arrive(smem_u32(&sm.dec[t][j & 1]));
         if (qt < g.nQ && p.skip_mask)
           p.skip_mask[((static_cast<size_t>(b) * p.H + h) * p.nQ + qt) * static_cast<size_t>(p.nK) + j] = skip ? 1 : 0;
       }
@@ -667,9 +653,9 @@ __device__ __forceinline__ void run_softmax(Smem& sm, uint32_t tmem, const FwdPa
   }
 }
 
-// One instance per feature set (packed documents, max_prob output, e4m3 scores, lambda = 0),
-// so that the plain fixed-length instance keeps the code generation of a kernel without them.
-template <bool kVarlen, bool kMaxProb, bool kFp8, bool kDense>
+// One instance per feature set (packed documents, max_prob output, e4m3 scores), so that the
+// plain fixed-length instance keeps the code generation of a kernel without them.
+template <bool kVarlen, bool kMaxProb, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     blasst_fwd_sm103a(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k,
@@ -703,8 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.v_full[s]), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
-      mbar_init(smem_u32(&sm.s_full[t][0]), 1);
-      mbar_init(smem_u32(&sm.s_full[t][1]), 1);
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
       mbar_init(smem_u32(&sm.dec[t][0]), 1);
       mbar_init(smem_u32(&sm.dec[t][1]), 1);
       mbar_init(smem_u32(&sm.p_ready[t]), kQTiles * kSoftmaxWarps);
@@ -732,15 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     regs_decrease<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer<kVarlen, kFp8, kDense>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
+      if (lane == 0) run_producer<kVarlen, kFp8>(sm, &tmap_q, &tmap_k, &tmap_v, p, g, h, qt0);
       __syncwarp();
     } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma<kVarlen, kFp8, kDense>(sm, sm.tmem_base, p, g);
-      __syncwarp();
+      run_mma<kVarlen, kFp8>(sm, sm.tmem_base, p, g);
     }
   } else {
     regs_increase<kSoftmaxRegs>();
-    run_softmax<kVarlen, kMaxProb, kDense>(sm, sm.tmem_base, p, g, b, h, qt0);
+    run_softmax<kVarlen, kMaxProb>(sm, sm.tmem_base, p, g, b, h, qt0);
   }
 
   tc_fence_before();
@@ -840,29 +824,24 @@ bool cached_bshd(CUtensorMap* map, const void* base, int B, int S, int H, bool e
 // The key tile whose copy the producer withholds (test of the bounded waits; -1: off).
 std::atomic<int> g_withhold_k{-1};
 
-// The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K,
-// 8 = lambda = 0 with bf16 scores; e4m3 scores at lambda = 0 run the general instance, which
-// measured faster for them).
+// The instance for feature bits (1 = packed documents, 2 = max_prob, 4 = e4m3 Q / K).
+// lambda = 0 runs the same instances: no tile passes the test and every one is kept.
 template <int kBits>
 const void* instance() {
   return reinterpret_cast<const void*>(
-      blasst_fwd_sm103a<(kBits & 1) != 0, (kBits & 2) != 0, (kBits & 4) != 0, (kBits & 8) != 0>);
+      blasst_fwd_sm103a<(kBits & 1) != 0, (kBits & 2) != 0, (kBits & 4) != 0>);
 }
-constexpr int kInstances = 12;
+constexpr int kInstances = 8;
 const void* kernel_for(int bits) {
-  switch (bits & 15) {
+  switch (bits & 7) {
     case 0: return instance<0>();
     case 1: return instance<1>();
     case 2: return instance<2>();
     case 3: return instance<3>();
-    case 4: case 12: return instance<4>();
-    case 5: case 13: return instance<5>();
-    case 6: case 14: return instance<6>();
-    case 7: case 15: return instance<7>();
-    case 8: return instance<8>();
-    case 9: return instance<9>();
-    case 10: return instance<10>();
-    default: return instance<11>();
+    case 4: return instance<4>();
+    case 5: return instance<5>();
+    case 6: return instance<6>();
+    default: return instance<7>();
   }
 }
 
@@ -990,10 +969,7 @@ blasst_status launch(const blasst_fwd_args& a) {
     return BLASST_ERR_LAUNCH;
   }
   void* args[] = {&tq, &tk, &tv, &p};
-  // lambda = 0 (factor 0, or one length below min_seq_len) can skip nothing: the bf16 instance
-  // for it neither publishes nor waits for decisions.
-  const bool dense = !(p.log2_lambda > -INFINITY) && !e4m3;
-  const void* kernel = kernel_for((varlen ? 1 : 0) | (a.max_prob ? 2 : 0) | (e4m3 ? 4 : 0) | (dense ? 8 : 0));
+  const void* kernel = kernel_for((varlen ? 1 : 0) | (a.max_prob ? 2 : 0) | (e4m3 ? 4 : 0));
   const cudaError_t e = cudaLaunchKernel(kernel,
                                          dim3((p.nQ + kQTiles - 1) / kQTiles, a.H, a.B), dim3(kThreads), args,
                                          kSmemBytes, st);

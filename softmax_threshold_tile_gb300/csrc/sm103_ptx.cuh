@@ -166,6 +166,61 @@ __device__ __forceinline__ void mma_ss_f8_off(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// Warp-wide forms: every lane of a converged warp executes them and `elect.sync` picks one
+// lane (the lowest, lane 0 when all 32 are present), which issues the instruction. The warp
+// stays converged, so the operands can live in uniform registers; issued from one lane inside a
+// branch the same MMAs took 90-115 cycles each on a GB300 against 64 in this form. Every MMA
+// and commit of a warp must go through these forms with all 32 lanes present, so that the
+// same lane issues them all (a commit tracks the MMAs of the thread that issues it).
+template <uint32_t kOffA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ss_off_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "add.u64 da, %1, %5;\n\t"
+      "add.u64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
+      : "memory");
+}
+
+template <uint32_t kOffA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ss_f8_off_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "add.u64 da, %1, %5;\n\t"
+      "add.u64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
+      : "memory");
+}
+
+template <uint32_t kOffB>
+__device__ __forceinline__ void mma_ts_off_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t.reg .b64 db;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "add.u64 db, %2, %5;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffB)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of this warp's 32 lanes, waited for before return.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

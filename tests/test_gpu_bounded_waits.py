@@ -33,7 +33,7 @@ def _gpu():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("factor", [2.0, 0.0])   # the general instance and the lambda = 0 one
+@pytest.mark.parametrize("factor", [2.0, 0.0])   # skipping, and lambda = 0
 @pytest.mark.parametrize("tile", [0, 1, 3])
 def test_withheld_key_tile_times_out_and_context_survives(tile, factor):
     import torch

@@ -55,7 +55,7 @@ def test_host_call_equals_device_call(B, H, Sq, Sk, hg, pinned):
 
 
 def test_host_call_at_factor_zero_equals_device_call():
-    """Factor 0 runs the lambda = 0 kernel instance inside the head-group pipeline."""
+    """Factor 0 (lambda = 0, nothing skipped) inside the head-group pipeline."""
     import torch
     import softmax_threshold_tile_gb300 as blasst
     B, H, Sq, Sk = 1, 6, 700, 900

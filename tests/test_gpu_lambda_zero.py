@@ -1,11 +1,11 @@
-"""The lambda = 0 kernel instance against the general one.
+"""Factor 0 (lambda = 0) against a factor too small to skip anything.
 
-With lambda = 0 no tile can be skipped, so for bf16 scores the library launches an instance
-that neither publishes nor waits for skip decisions (the producer copies every V tile and the
-MMA thread issues every P . V). Its arithmetic is the general instance's: run with a factor so small that
-the skip test cannot pass (ln lambda below -85 while score gaps stay within a few tens), the
-general instance must return bit-identical outputs. Both are also checked against the oracle
-by the parity tests at factor 0."""
+With lambda = 0 the threshold ln(lambda) is -inf, so no row passes the skip test and every key
+tile is kept; the kernel takes the same path as for any other factor. A factor so small that
+the test cannot pass either (ln lambda below -85 while score gaps stay within a few tens) must
+therefore give bit-identical outputs, for bf16 and e4m3 scores, fixed-length batches, packed
+documents, and the min_seq_len gate (which turns lambda to 0 on the host). Both are also
+checked against the oracle by the parity tests at factor 0."""
 import math
 
 import numpy as np
@@ -16,7 +16,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-TINY_FACTOR = 2e-38  # general instance, nothing skippable
+TINY_FACTOR = 2e-38  # nothing skippable
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,29 +53,28 @@ def _same(a, b):
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk", [(2, 3, 1000, 1000), (1, 2, 300, 1000), (1, 1, 1, 129), (1, 2, 129, 8)])
-def test_dense_instance_equals_general_bf16(B, H, Sq, Sk):
+def test_factor_zero_equals_tiny_factor_bf16(B, H, Sq, Sk):
     q, k, v = parity.clustered_inputs(B, H, Sq, Sk, seed=Sq + 3 * Sk)
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
-    dense = _blasst().attn_fwd(qd, kd, vd, 0.0, want_mask=True, want_max_prob=True)
-    general = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR, want_mask=True, want_max_prob=True)
-    _same(dense, general)
-    assert int(dense.skip_mask.sum()) == 0 and int(general.skip_mask.sum()) == 0
+    zero = _blasst().attn_fwd(qd, kd, vd, 0.0, want_mask=True, want_max_prob=True)
+    tiny = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR, want_mask=True, want_max_prob=True)
+    _same(zero, tiny)
+    assert int(zero.skip_mask.sum()) == 0 and int(tiny.skip_mask.sum()) == 0
 
 
-def test_dense_instance_equals_general_wan_heads():
+def test_factor_zero_equals_tiny_factor_wan_heads():
     """Full Wan length (the benchmark's launch shape per head) on four heads."""
     w = synth.WORKLOADS["wan_32760"]
     q, k, v = synth.make_qkv(w)
     heads = [0, 13, 26, 39]
     qd, kd, vd = (parity.to_device(np.ascontiguousarray(x[:, :, heads])) for x in (q, k, v))
-    dense = _blasst().attn_fwd(qd, kd, vd, 0.0)
-    general = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR)
-    _same(dense, general)
+    zero = _blasst().attn_fwd(qd, kd, vd, 0.0)
+    tiny = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR)
+    _same(zero, tiny)
 
 
 def test_fp8_factor_zero_equals_tiny_factor():
-    """e4m3 scores at lambda = 0 run the general instance (it measured faster for them than the
-    lambda = 0 one); with nothing skippable the two factors give the same bits."""
+    """e4m3 scores: with nothing skippable the two factors give the same bits."""
     import torch
     if not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("torch without float8_e4m3fn")
@@ -83,12 +82,12 @@ def test_fp8_factor_zero_equals_tiny_factor():
     q8, dq = synth.quantize_e4m3(q)
     k8, dk = synth.quantize_e4m3(k)
     qd, kd, vd = parity.to_device_e4m3(q8), parity.to_device_e4m3(k8), parity.to_device(v)
-    dense = _blasst().attn_fwd(qd, kd, vd, 0.0, q_descale=dq, k_descale=dk)
-    general = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR, q_descale=dq, k_descale=dk)
-    _same(dense, general)
+    zero = _blasst().attn_fwd(qd, kd, vd, 0.0, q_descale=dq, k_descale=dk)
+    tiny = _blasst().attn_fwd(qd, kd, vd, TINY_FACTOR, q_descale=dq, k_descale=dk)
+    _same(zero, tiny)
 
 
-def test_dense_instance_equals_general_packed_documents():
+def test_factor_zero_equals_tiny_factor_packed_documents():
     import torch
     lens = [1000, 37, 2048, 129, 1]
     qs, ks, vs = [], [], []
@@ -99,14 +98,14 @@ def test_dense_instance_equals_general_packed_documents():
     cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
     m = max(lens)
-    dense = _blasst().attn_varlen_fwd(qd, kd, vd, cu, cu, m, m, 0.0, want_max_prob=True)
-    general = _blasst().attn_varlen_fwd(qd, kd, vd, cu, cu, m, m, TINY_FACTOR, want_max_prob=True)
-    _same(dense, general)
+    zero = _blasst().attn_varlen_fwd(qd, kd, vd, cu, cu, m, m, 0.0, want_max_prob=True)
+    tiny = _blasst().attn_varlen_fwd(qd, kd, vd, cu, cu, m, m, TINY_FACTOR, want_max_prob=True)
+    _same(zero, tiny)
 
 
-def test_min_seq_len_above_the_length_runs_the_dense_instance():
-    """One length below min_seq_len: the host turns lambda to 0 and launches the dense instance;
-    its outputs equal the factor-0 call's and nothing is skipped, whatever the factor."""
+def test_min_seq_len_above_the_length_runs_dense():
+    """One length below min_seq_len: the host turns lambda to 0; the outputs equal the factor-0
+    call's and nothing is skipped, whatever the factor."""
     q, k, v = parity.clustered_inputs(1, 2, 1000, 1000, seed=5)
     qd, kd, vd = (parity.to_device(x) for x in (q, k, v))
     gated = _blasst().attn_fwd(qd, kd, vd, 64.0, min_seq_len=1001, want_mask=True)

@@ -2,7 +2,7 @@
 every pipeline hand-off is an ordered barrier, so repeated calls on the same inputs must give
 the same bits (o, lse, max_prob, skip counts and mask). A missing fence or a stage reused too
 early in the warp-specialised pipeline would show here as a run-to-run difference, on the
-general instance (skipping), the lambda = 0 instance and the e4m3 score product."""
+bf16 scores with and without skipping (factor 0) and the e4m3 score product."""
 import pytest
 
 import synth
