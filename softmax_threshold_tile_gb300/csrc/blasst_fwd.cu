@@ -665,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt0 = blockIdx.x * kQTiles, h = blockIdx.y, b = blockIdx.z;
+  // Blocks start in blockIdx.x order: the last query tiles, which keep the longest prefix of key
+  // tiles when the test skips, go first, so the short ones fill the last wave.
+  const int qt0 = (gridDim.x - 1 - blockIdx.x) * kQTiles, h = blockIdx.y, b = blockIdx.z;
   const Geo g = make_geo<kVarlen>(p, b, h);
   if (qt0 * kTile >= g.Sq) return;  // a packed document shorter than this CTA's first row
   if (g.Sk == 0) {
