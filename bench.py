@@ -44,6 +44,7 @@ NCU_TRAFFIC = {
     "265a36ec00c0eed3": {"workload": "wan_32760", "factor": 32.0, "bytes": 1008250112 + 322755328},
     "f126bb95c3f763e9": {"workload": "wan_32760", "factor": 32.0, "bytes": 1007854848 + 322692096},
     "d55dd674df77d3f0": {"workload": "wan_32760", "factor": 32.0, "bytes": 1008416512 + 322506496},
+    "2fc024e7b09c30be": {"workload": "wan_32760", "factor": 32.0, "bytes": 1007930880 + 320723200},
 }
 UNIT = "TFLOPS (dense-equivalent)"
 TILE = 128
