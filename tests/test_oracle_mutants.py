@@ -34,6 +34,13 @@ MUTANTS = {
     "inverted_test": ("(worst < ln_lambda)", "(worst > ln_lambda)"),
     # max_prob as l instead of 1 / l
     "max_prob_inverted": ("= 1.0 / l[i];", "= l[i];"),
+    # a non-strict test: a gap equal to ln(lambda) would skip ("Algorithm": strictly below)
+    "non_strict_test": ("(worst < ln_lambda)", "(worst <= ln_lambda)"),
+    # a skipped tile raises the running max ("Algorithm": a skipped tile changes nothing);
+    # visible only for lambda > 1, where a skipped tile's maximum can exceed it
+    "skipped_tile_moves_max": ("continue; /* the tile's contribution to l and O is omitted */",
+                               "{ for (int i2 = 0; i2 < nr; ++i2) if (tile_max[i2] > m[i2]) m[i2] = tile_max[i2]; "
+                               "continue; }"),
 }
 
 

@@ -12,31 +12,24 @@ Each check below would fail on a plausible mistake in ``oracle/blasst_oracle.c``
    skip_j = [max_i (tile_max_j[i] - M_{j-1}[i]) < ln(lambda)]. Scores for this
    check come from numpy, not from the oracle.
 3. Monotone skip sets in lambda (follows from 2).
-4. A hand-built case with exactly representable scores skips exactly the
-   predicted tiles (tests/golden/hand_built_tiles.json) and has a closed-form output.
+4. Hand-built cases with exactly representable scores skip exactly the
+   predicted tiles and have closed-form outputs (tests/hand_built.py and its golden
+   files): the all-rows rule, a query tail, a gap of exactly ln(lambda) = 0 (the test
+   is strict), and lambda > 1 with a skipped tile above the running max (a skipped
+   tile does not move it).
 5. The output error stays within the bound implied by the skipped mass:
    |O_skip - O_dense| <= delta * (max_k v - min_k v) per column, and
    delta < lambda * (number of skipped keys in the row)
    ("Algorithm": exp(tile_max - running_max) bounds every key weight of the tile).
 """
-import json
 import math
-import os
 
 import numpy as np
 import pytest
 
 import oracle
 import synth
-
-GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-
-
-def hadamard(n):
-    h = np.array([[1]], dtype=np.int64)
-    while h.shape[0] < n:
-        h = np.block([[h, h], [h, -h]])
-    return h
+from tests import hand_built
 
 
 def random_bf16(shape, seed, scale=1.0):
@@ -191,54 +184,28 @@ def test_skip_set_monotone_in_lambda(name, S, H):
     assert counts[0] == 0
 
 
-def _hand_built(Sq):
-    d, Sk = 128, 520
-    h = hadamard(128)
-    q = np.zeros((1, Sq, 1, d), np.float32)
-    q[0, :, 0] = h[:Sq]
-    k = np.zeros((1, Sk, 1, d), np.float32)
-    k[0, :128, 0] = 2 * h
-    k[0, 256, 0] = 2 * h[5]
-    c = np.arange(Sk)[:, None]
-    t = np.arange(d)[None, :]
-    vv = ((7 * c + 3 * t) % 5 - 2).astype(np.float32)
-    v = vv[None, :, None, :].copy()
-    conv = synth.f32_to_bf16_bits
-    return conv(q), conv(k), conv(v), vv.astype(np.float64)
-
-
 def _load_golden():
-    with open(os.path.join(GOLDEN, "hand_built_tiles.json")) as fh:
-        return json.load(fh)["cases"]
+    return hand_built.load_cases()
 
 
-@pytest.mark.parametrize("case", _load_golden(), ids=lambda c: f"Sq{c['Sq']}_lnlam{c['ln_lambda']}")
+@pytest.mark.parametrize("case", _load_golden(), ids=hand_built.case_id)
 def test_hand_built_case_skips_predicted_tiles(case):
-    Sq, Sk = case["Sq"], case["Sk"]
-    q, k, v, vv = _hand_built(Sq)
-    ln_lam = float(case["ln_lambda"])
-    factor = 0.0 if ln_lam == -math.inf else Sk * math.exp(ln_lam)
-    scale = 1.0 / math.sqrt(128)
-    res = oracle.skip_softmax_attn(q, k, v, scale, factor)
-    assert res["mask"][0].tolist() == case["mask"]
-    if "gap" in case:
-        expect = [float(x) for x in case["gap"]]
+    """Masks (and the recorded gaps) of the hand-built cases, and their closed-form outputs.
+
+    The "above_one" construction has lambda > 1: a skipped tile whose maximum exceeds the
+    running max must leave it unchanged, which decides the next tile."""
+    name, c = case
+    q, k, v, vv = hand_built.build(name, c["Sq"])
+    res = oracle.skip_softmax_attn(q, k, v, hand_built.SCALE, hand_built.factor_of(c))
+    assert res["mask"][0].tolist() == c["mask"]
+    if "gap" in c:
+        expect = [float(x) for x in c["gap"]]
         np.testing.assert_allclose(res["gap"][0], expect, rtol=0, atol=1e-12)
-    if case["mask"] == [0, 1, 0, 1, 1]:
-        # closed-form output over the kept keys (tiles 0 and 2)
-        E = math.exp(256 * scale)
-        tile0, tile2 = vv[0:128], vv[256:384]
-        for i in range(Sq):
-            if i != 5:
-                num = E * tile0[i] + (tile0.sum(0) - tile0[i]) + tile2.sum(0)
-                den = E + 127 + 128
-                lse = 256 * scale + math.log(1 + 255 / E)   # ln(E + 255)
-            else:
-                num = E * tile0[5] + E * tile2[0] + (tile0.sum(0) - tile0[5]) + (tile2.sum(0) - tile2[0])
-                den = 2 * E + 127 + 127
-                lse = 256 * scale + math.log(2 + 254 / E)   # ln(2E + 254)
-            np.testing.assert_allclose(res["o"][0, i], num / den, rtol=0, atol=1e-13)
-            assert abs(res["lse"][0, i] - lse) < 1e-12
+    expected = hand_built.closed_form(name, c, vv)
+    if expected is not None:
+        o_ref, lse_ref = expected
+        np.testing.assert_allclose(res["o"][0, :c["Sq"]], o_ref, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(res["lse"][0, :c["Sq"]], lse_ref, rtol=0, atol=1e-12)
 
 
 @pytest.mark.parametrize("name,S,H,factors", [
